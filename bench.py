@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark: effective (unmasked-FLOP) TFLOP/s of column-wise-masked exact
+attention, forward + backward, on one GB300 per process.
+
+One step = the whole hot path over one batch of synthetic input already in
+HBM: tile classification, forward, backward preprocess, backward main and the
+dQ conversion. The default workload is B=1, H=32, N=32768, d=128 with a causal
+document mask (document lengths uniform in [512, 8192], seed 0). Q, K, V and
+dO (1.07 GB together) are larger than the 129 MB L2, so no flush is needed
+between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Under torchrun each rank runs an independent replica (no collective on the
+data path) and rank 0 prints one JSON line with the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective TFLOP/s (unmasked FLOPs) fwd+bwd at 1 GB300; % of dense BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+# DRAM bytes per launch of the backward main kernel from an ncu capture (see
+# profiles/), valid only for the kernel source it was measured on.
+NCU_TRAFFIC = {}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash(files=("bwd.cu", "ptx.cuh")) -> str:
+    h = hashlib.sha1()
+    for f in files:
+        with open(os.path.join(ROOT, "mask_aware_exact_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ native arm
+def run_native(args):
+    import torch
+
+    from mask_aware_exact_gb300 import build as libbuild
+    from mask_aware_exact_gb300 import flashmask as fm
+    from mask_aware_exact_gb300 import flops as F
+    from mask_aware_exact_gb300 import replicas as R
+    from mask_aware_exact_gb300 import workloads as W
+
+    rank, world, local = R.world()
+    torch.cuda.set_device(local)
+    R.init("nccl")
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        libbuild.build()
+    R.barrier()
+    fm.load()
+
+    w = W.workload(args.workload)
+    if args.heads:
+        w.H = args.heads
+        w.name += f"_h{args.heads}"
+    B, H, N, d = w.B, w.H, w.N, w.d
+    scale = 1.0 / math.sqrt(d)
+    q_h, k_h, v_h, do_h = (x.pin_memory() for x in W.make_qkv(B, H, N, d, w.seed))
+    q, k, v, do = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
+    mask = fm.DeviceMask.from_spec(w.mask, device=dev)
+    Hm = mask.Hm
+    ws = fm.alloc_workspace(B, H, Hm, N, d, for_bwd=True, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fl = F.effective_flops(w.mask, H, d)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fm.flashmask_classify(mask, B, N, ws)
+        if ev is not None:
+            ev[1].record(stream)
+        fm.flashmask_fwd(q, k, v, mask, ws, scale=scale, o=o, lse=lse, ws_classified=True)
+        if ev is not None:
+            ev[2].record(stream)
+        fm.flashmask_bwd_preprocess(o, lse, do, Hm, ws)
+        if ev is not None:
+            ev[3].record(stream)
+        fm.flashmask_bwd_main(q, k, v, do, mask, ws, dk, dv, scale=scale)
+        if ev is not None:
+            ev[4].record(stream)
+        fm.flashmask_bwd_finalize(dq, Hm, ws, scale=scale)
+        if ev is not None:
+            ev[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    st, site = fm.flashmask_check_status(ws)
+    if st != fm.FM_OK:
+        raise RuntimeError(f"device status {st} at site {site} during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    R.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    R.barrier()
+    clk = clocks.stop()
+    elapsed_s = t0.elapsed_time(t1) / 1e3
+    st, site = fm.flashmask_check_status(ws)
+    if st != fm.FM_OK:
+        raise RuntimeError(f"device status {st} at site {site} in the timed region")
+    names = ["classify", "fwd", "bwd_pre", "bwd_main", "bwd_finalize"]
+    per = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(names)}
+    agg = R.aggregate_throughput(fl["total"] * K, elapsed_s, dev)
+    value = agg["throughput"] / 1e12
+    ms_per_step = agg["max_elapsed_s"] / K * 1e3
+
+    # ---------------- end to end: pinned host buffers in, results back to host
+    out_h = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+             for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    mask_h = {n: getattr(mask, n).cpu().pin_memory() for n in ("lts", "lte", "uts", "ute")
+              if getattr(mask, n) is not None}
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, do_h)) + \
+        sum(t.numel() * t.element_size() for t in mask_h.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+
+    def e2e_step():
+        for dst, src in ((q, q_h), (k, k_h), (v, v_h), (do, do_h)):
+            dst.copy_(src, non_blocking=True)
+        for n, t in mask_h.items():
+            getattr(mask, n).copy_(t, non_blocking=True)
+        fm.flashmask_fwd(q, k, v, mask, ws, scale=scale, o=o, lse=lse, ws_classified=False)
+        fm.flashmask_bwd(q, k, v, o, lse, do, mask, ws, scale=scale, dq=dq, dk=dk, dv=dv,
+                         ws_classified=True)
+        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            out_h[n].copy_(t, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    K2 = max(3, K // 2)
+    R.barrier()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    R.barrier()
+    e2e_s = a0.elapsed_time(a1) / 1e3
+    e2e_agg = R.aggregate_throughput(fl["total"] * K2, e2e_s, dev)
+    st, site = fm.flashmask_check_status(ws)
+    if st != fm.FM_OK:
+        raise RuntimeError(f"device status {st} at site {site} in the end-to-end region")
+
+    pk, pk_src = peaks()
+    peak_dense = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    peak_sust = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # dominant kernel: the backward main kernel (largest share of the step)
+    dom = max(("fwd", "bwd_main"), key=lambda n: per[n])
+    dom_flops = fl["bwd"] if dom == "bwd_main" else fl["fwd"]
+    achieved = dom_flops / (per[dom] / 1e3) / 1e12
+    src_hash = kernel_source_hash(("bwd.cu", "ptx.cuh") if dom == "bwd_main" else ("fwd.cu", "ptx.cuh"))
+    traffic = NCU_TRAFFIC.get(f"{dom}@{src_hash}")
+
+    result = None
+    if rank == 0:
+        result = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "description": w.description, "B": B, "H": H, "N": N,
+                       "d": d, "global_batch": B * world, "seq_len": N,
+                       "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                       "l2": "inputs (Q,K,V,dO = %.2f GB) larger than L2; no flush" %
+                             (4 * q.numel() * 2 / 1e9),
+                       "nnz_per_replica": fl["nnz"],
+                       "flops_per_step_per_replica": fl["total"]},
+            "pct_of_peak": round(100 * value / world / peak_dense, 2),
+            "peak_bf16_tflops": peak_dense,
+            "peak_source": pk_src,
+            "kernels_ms": {n: round(per[n], 4) for n in names},
+            "fwd_tflops": round(fl["fwd"] / (per["fwd"] / 1e3) / 1e12, 1),
+            "bwd_tflops": round(fl["bwd"] / ((per["bwd_pre"] + per["bwd_main"] + per["bwd_finalize"])
+                                             / 1e3) / 1e12, 1),
+            "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
+                         "peak": peak_sust, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak_sust, 4),
+                         "peak_kind": f"bf16 sustained ({pk_src})",
+                         "traffic": traffic},
+            "e2e": {"value": round(e2e_agg["throughput"] / 1e12, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "ms_per_step": round(e2e_agg["max_elapsed_s"] / K2 * 1e3, 4)},
+            "gpu_launches": 7 * K,
+            "clocks": clk,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(w, args.oracle_seconds)
+    R.finalize()
+    return result
+
+
+# ------------------------------------------------------------------ oracle (CPU) leg
+def _oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(w, seconds: float) -> dict:
+    """The fp64 oracle (as it stands) on the host cores over a bounded sample of
+    the same workload: whole 128-row query blocks of head (0, 0), spread evenly
+    over the sequence, processed until about `seconds` have elapsed. Effective
+    FLOPs are counted exactly as for the GPU (14*d per visible entry)."""
+    from oracle import attention as A
+    import torch  # noqa: F401  (make_qkv returns torch tensors)
+    from mask_aware_exact_gb300 import workloads as W
+
+    q, k, v, do = (x[0, 0].float().numpy().astype(np.float64)
+                   for x in W.make_qkv(1, 1, w.N, w.d, w.seed))
+    m = w.mask
+    g = lambda a: None if a is None else a[0, 0]
+    b = (g(m.lts), g(m.lte), g(m.uts), g(m.ute))
+    scale = 1 / math.sqrt(w.d)
+    Tr = w.N // 128
+    order = np.argsort((np.arange(Tr) * 0.6180339887) % 1.0)  # evenly spread blocks
+    flops = 0
+    t0 = time.perf_counter()
+    used = 0
+    for r in order:
+        rows = np.arange(r * 128, r * 128 + 128)
+        A.backward_head(q, k, v, do, *b, m.causal, scale, rows=rows)
+        nnz = int(A.visible(rows, w.N, *b, m.causal).sum())
+        flops += 14 * w.d * nnz
+        used += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": flops / el / 1e12, "unit": UNIT, "cores": _oracle_threads(), "kind": "oracle",
+            "sample": f"{used} of {Tr} query blocks of head (0,0) of {w.name}, fwd+bwd fp64 "
+                      f"NumPy, {el:.1f} s; value scaled to TFLOP/s of effective FLOPs"}
+
+
+def run_reference(args):
+    from mask_aware_exact_gb300 import replicas as R
+    from mask_aware_exact_gb300 import workloads as W
+
+    rank, world, _ = R.world()
+    if rank != 0:
+        return None
+    w = W.workload(args.workload)
+    per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, per_step / 4)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(w, per_step))
+    el = time.perf_counter() - t0
+    value = statistics.mean(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = value
+    cb["sample"] = f"each step: {cb['sample']}"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "description": w.description, "B": w.B, "H": w.H,
+                       "N": w.N, "d": w.d},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", type=int, default=2, help="synthetic workload index 0..4")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-seconds", type=float, default=12.0)
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override H (profiling captures on a smaller case only; not a bench line)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "native" else args.warmup
+    res = run_reference(args) if args.impl == "reference" else run_native(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

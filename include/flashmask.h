@@ -1,0 +1,164 @@
+/*
+ * flashmask.h: C ABI of the column-wise-masked exact attention library
+ * (libflashmask.so, sm_103a).
+ *
+ * What it computes ("FlashMask: Efficient and Rich Mask Extension of
+ * FlashAttention", abstract; "FlashMask-3: ... Mask-Aware Distributed
+ * Attention", abstract): exact scaled-dot-product attention, forward and
+ * backward, under a mask stored column-wise as four int32 query-axis boundary
+ * vectors per key column. For key column j, query row i is MASKED when
+ *
+ *     (causal && j > i) || (LTS[j] <= i < LTE[j]) || (UTS[j] <= i < UTE[j])
+ *
+ * Intervals are half-open; an interval whose start >= end masks nothing, and
+ * bounds outside [0, N] act as if clamped to [0, N]. Over visible entries:
+ *
+ *     S = scale * Q K^T,  P = softmax_rows(S),  O = P V,  LSE = rowwise ln sum exp(S)
+ *
+ * A query row with no visible key gets O = 0 and LSE = -inf; it contributes
+ * nothing to any gradient. The backward returns dQ, dK, dV for an upstream
+ * gradient dO (the FlashAttention recomputation scheme: P is rebuilt from Q, K
+ * and LSE; D = rowsum(dO * O)).
+ *
+ * Layouts (all row-major, contiguous, device memory owned by the caller):
+ *   Q, K, V, O, dO, dQ, dK, dV : bf16  [B, H, N, d]
+ *   LSE                        : fp32  [B, H, N]     (natural log)
+ *   LTS, LTE, UTS, UTE         : int32 [B, Hm, N]    (head h reads mask head h / (H / Hm))
+ * Supported shapes: d in {64, 128}; N a positive multiple of 128; H % Hm == 0;
+ * B * H * N < 2^31. Other shapes return FM_ERR_UNSUPPORTED.
+ *
+ * Workspace: the library never allocates. The caller passes one device buffer
+ * of at least flashmask_workspace_bytes(...) bytes, aligned to 256 bytes. It
+ * holds the tile classification (written by flashmask_classify), the backward's
+ * fp32 scratch and a device status word. One workspace must not be used by two
+ * calls that may run at the same time.
+ *
+ * Streams and errors: every call validates its arguments on the host and
+ * returns an error WITHOUT launching anything if they are bad. Otherwise it
+ * enqueues kernels on `stream` (a cudaStream_t, NULL for the legacy default
+ * stream) and returns FM_OK without synchronising. Every wait inside a kernel
+ * is bounded in time; a kernel whose wait gives up records the failure in the
+ * workspace status word and exits. flashmask_check_status() reads and clears
+ * that word.
+ */
+#ifndef FLASHMASK_H
+#define FLASHMASK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FM_OK = 0,
+  FM_ERR_INVALID_ARG = 1,  /* null pointer, negative size, scale not finite, ...   */
+  FM_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, N % 128 != 0, H % Hm != 0, ...    */
+  FM_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed          */
+  FM_ERR_TIMEOUT = 4,      /* a kernel wait gave up (see flashmask_check_status)   */
+  FM_ERR_WORKSPACE = 5     /* workspace null, misaligned or smaller than required  */
+} fm_status;
+
+/* Tile edge (rows and columns) of the classification. */
+#define FM_TILE 128
+
+/* Three-way tile label ("FlashMask" abstract: skip the computation that the
+ * mask makes unnecessary). */
+#define FM_TILE_NONE 0    /* no entry of the tile is masked: no mask work        */
+#define FM_TILE_PARTIAL 1 /* some entries masked: mask applied element by element */
+#define FM_TILE_FULL 2    /* every entry masked: the tile is skipped             */
+
+/* The column-wise mask: device pointers to int32 [B, Hm, N] vectors.
+ * uts and ute may both be NULL (no upper interval). */
+typedef struct {
+  const int32_t* lts;
+  const int32_t* lte;
+  const int32_t* uts;
+  const int32_t* ute;
+  int Hm;     /* number of mask heads, 1 <= Hm <= H, H % Hm == 0 */
+  int causal; /* nonzero: also mask j > i                         */
+} fm_mask;
+
+/* Byte offsets of the workspace regions (from the workspace base), for callers
+ * that want to read the classification. Regions marked [bwd] exist only when
+ * the workspace was sized with for_bwd != 0 (otherwise their offsets are 0).
+ *   status    int32[4]                   device status word (0 = OK) + detail
+ *   minmax    int32  [B,Hm,Tc,8]         per key block: min/max of LTS, LTE, UTS, UTE
+ *   labels    uint8  [B,Hm,Tr,Tc]        tile label, query-block major
+ *   labels_t  uint8  [B,Hm,Tc,Tr]        tile label, key-block major
+ *   row_count int32  [B,Hm,Tr]           non-FULL tiles per query block
+ *   row_list  int32  [B,Hm,Tr,Tc]        (key block << 2) | label, ascending
+ *   row_order int32  [B,Hm,Tr]           query blocks by descending row_count
+ *   col_count int32  [B,Hm,Tc]           non-FULL tiles per key block
+ *   col_list  int32  [B,Hm,Tc,Tr]        (query block << 2) | label, ascending
+ *   col_order int32  [B,Hm,Tc]           key blocks by descending col_count
+ *   lse2      fp32   [B,H,N]      [bwd]  LSE * log2(e) (+inf for a fully masked row)
+ *   delta     fp32   [B,H,N]      [bwd]  rowsum(dO * O)
+ *   dq_accum  fp32   [B,H,N,d]    [bwd]  dQ accumulator
+ * with Tr = Tc = N / 128. */
+typedef struct {
+  size_t status, minmax, labels, labels_t, row_count, row_list, row_order, col_count, col_list,
+      col_order, lse2, delta, dq_accum, total;
+} fm_ws_layout;
+
+/* Workspace size in bytes for the given problem; 0 for an unsupported shape. */
+size_t flashmask_workspace_bytes(int B, int H, int Hm, int N, int d, int for_bwd);
+
+/* Fills *out with the region offsets described above. */
+fm_status flashmask_workspace_layout(int B, int H, int Hm, int N, int d, int for_bwd,
+                                     fm_ws_layout* out);
+
+/* Tile classification pre-pass: reduces the boundary vectors to the per-key-block
+ * min/max table, the exact three-way label of every (query block, key block)
+ * tile, the compacted non-FULL lists and the descending-work orders, all in the
+ * workspace. Reads 16*B*Hm*N bytes. Asynchronous on `stream`. */
+fm_status flashmask_classify(const fm_mask* mask, int B, int N, void* ws, size_t ws_bytes,
+                             void* stream);
+
+/* Forward: O [B,H,N,d] bf16 and LSE [B,H,N] fp32 from Q, K, V. `scale`
+ * multiplies Q K^T (pass 1/sqrt(d) for standard attention). If
+ * ws_classified == 0 the call runs flashmask_classify first; pass 1 to reuse a
+ * classification of the same mask already in `ws`. Asynchronous on `stream`. */
+fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_mask* mask, int B,
+                        int H, int N, int d, float scale, void* o, float* lse, void* ws,
+                        size_t ws_bytes, int ws_classified, void* stream);
+
+/* Backward: dQ, dK, dV [B,H,N,d] bf16 from Q, K, V, the forward's O and LSE,
+ * and the upstream gradient dO. The workspace must be sized with for_bwd != 0.
+ * ws_classified as in flashmask_fwd. Asynchronous on `stream`. */
+fm_status flashmask_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, const fm_mask* mask, int B, int H,
+                        int N, int d, float scale, void* dq, void* dk, void* dv, void* ws,
+                        size_t ws_bytes, int ws_classified, void* stream);
+
+/* The three stages flashmask_bwd runs after the (optional) classification,
+ * exposed so that a caller can schedule or time them separately. They must run
+ * in this order on one stream with one workspace:
+ *   preprocess: D = rowsum(dO * O), lse2 = LSE * log2(e), dQ accumulator = 0
+ *               (HBM-bound; reads O and dO, writes 4*(2+d)*B*H*N bytes).
+ *   main:       dK, dV and the fp32 dQ accumulator over every non-FULL tile
+ *               (needs a classification of `mask` and the preprocess output).
+ *   finalize:   dQ = bf16(scale * accumulator).
+ * Hm is the mask's number of heads (it fixes the workspace layout). */
+fm_status flashmask_bwd_preprocess(const void* o, const float* lse, const void* dout, int B, int H,
+                                   int Hm, int N, int d, void* ws, size_t ws_bytes, void* stream);
+fm_status flashmask_bwd_main(const void* q, const void* k, const void* v, const void* dout,
+                             const fm_mask* mask, int B, int H, int N, int d, float scale,
+                             void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+fm_status flashmask_bwd_finalize(int B, int H, int Hm, int N, int d, float scale, void* dq,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then reads and clears the workspace status word.
+ * Returns FM_ERR_TIMEOUT if a kernel wait gave up since the last check,
+ * FM_ERR_CUDA if the stream reports an error, FM_OK otherwise. If detail is
+ * not NULL it receives the recorded failure site (0 if none). */
+fm_status flashmask_check_status(void* ws, void* stream, int* detail);
+
+/* Static description of a status code. */
+const char* flashmask_status_string(fm_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLASHMASK_H */

@@ -1,0 +1,533 @@
+// Backward kernels ("FlashMask: Efficient and Rich Mask Extension of
+// FlashAttention", abstract: exact forward and backward that skip masked
+// work; the gradient recomputes P from Q, K and the saved LSE as in the
+// FlashAttention family):
+//
+//   bwd_pre     D_i = <dO_i, O_i> (fp32), lse2_i = LSE_i * log2(e) (+inf for a
+//               fully masked row, so its P is exactly 0), dQ accumulator = 0.
+//   bwd_kernel  one CTA per (batch, head, key block of 128 keys), looping over
+//               the non-FULL query blocks of that key block:
+//                 S^T  = K Q^T              (tcgen05, TMEM)
+//                 dP^T = V dO^T             (tcgen05, TMEM)
+//                 P^T  = exp2(S^T c - lse2) masked on PARTIAL tiles -> bf16 in TMEM
+//                 dV  += P^T dO             (A from TMEM)
+//                 dS^T = P^T (dP^T - D)     -> bf16 in shared memory
+//                 dK  += dS^T Q             (dS^T K-major)
+//                 dQ_t = dS K               (dS^T read MN-major) -> TMEM
+//               dQ_t leaves TMEM through the tile's own Q/dO stage buffers (free
+//               once its MMAs are done) and a TMA bulk reduce-add into the
+//               global fp32 accumulator.
+//   dq_convert  dQ = bf16(scale * accumulator).
+//
+// Warp roles of bwd_kernel: warps 0-3 compute (thread t = key t = TMEM lane t),
+// warps 4-7 drain dQ_t (thread t = query t), warp 8 TMA producer, warp 9 MMA
+// issuer.
+//
+// TMEM columns (512): S^T / P^T [0,128)  dP^T / dQ_t [128,256)
+//                     dV [256, 256+d)    dK [384, 384+d)
+#include "internal.h"
+#include "ptx.cuh"
+#include "../../include/flashmask.h"
+
+namespace fm {
+
+namespace {
+
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kDS = kV + kTileBytes;           // 128 keys x 128 queries bf16
+  static constexpr int kQ = kDS + kTile * kTile * 2;    // 2 stages
+  static constexpr int kDO = kQ + 2 * kTileBytes;       // 2 stages
+  static constexpr int kLse = kDO + 2 * kTileBytes;     // fp32[2][128]
+  static constexpr int kDelta = kLse + 2 * kTile * 4;   // fp32[2][128]
+  static constexpr int kBar = kDelta + 2 * kTile * 4;
+  // kv_full, q_full[2], q_empty[2], s_full, dp_full, pt_ready, ds_ready, dv_done,
+  // tile_done, dq_drained
+  static constexpr int kNumBars = 12;
+  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kBytes = kTmemSlot + 16;
+};
+
+struct BwdBars {
+  uint32_t base;
+  __device__ uint32_t kv_full() const { return base; }
+  __device__ uint32_t q_full(int s) const { return base + 8 * (1 + s); }
+  __device__ uint32_t q_empty(int s) const { return base + 8 * (3 + s); }
+  __device__ uint32_t s_full() const { return base + 8 * 5; }
+  __device__ uint32_t dp_full() const { return base + 8 * 6; }
+  __device__ uint32_t pt_ready() const { return base + 8 * 7; }
+  __device__ uint32_t ds_ready() const { return base + 8 * 8; }
+  __device__ uint32_t dv_done() const { return base + 8 * 9; }
+  __device__ uint32_t tile_done() const { return base + 8 * 10; }
+  __device__ uint32_t dq_drained() const { return base + 8 * 11; }
+};
+
+__device__ __forceinline__ void record_failure(int32_t* status, int bit, int site) {
+  atomicOr(&status[0], bit);
+  atomicCAS(&status[1], 0, site);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Adds a shared-memory box into global memory through a tensor map (fp32 add).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x,
+                                                  int y) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::
+          "l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void drain_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- preprocess
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
+                                                      const uint16_t* __restrict__ dout,
+                                                      const float* __restrict__ lse,
+                                                      float* __restrict__ delta,
+                                                      float* __restrict__ lse2,
+                                                      float* __restrict__ dq_accum,
+                                                      long long rows) {
+  constexpr int kThreadsPerRow = D / 8;  // 8 bf16 (16 bytes) per thread
+  const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = gt / kThreadsPerRow;
+  const int part = static_cast<int>(gt % kThreadsPerRow);
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
+    const uint4 g = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
+    const uint32_t* ap = reinterpret_cast<const uint32_t*>(&a);
+    const uint32_t* gp = reinterpret_cast<const uint32_t*>(&g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(ap[i] << 16), __uint_as_float(gp[i] << 16), acc);
+      acc = fmaf(__uint_as_float(ap[i] & 0xffff0000u), __uint_as_float(gp[i] & 0xffff0000u), acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dq_accum + row * D + part * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = kThreadsPerRow / 2; off > 0; off >>= 1)
+    acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) {
+    delta[row] = acc;
+    const float L = lse[row];
+    lse2[row] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+  }
+}
+
+// ---------------------------------------------------------------- main
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+               const __grid_constant__ CUtensorMap mdq, const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int BH = p.B * p.H;
+  const int rank = blockIdx.x / BH, bh = blockIdx.x % BH;
+  const int b = bh / p.H, h = bh % p.H;
+  const int bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
+  const int kb = p.col_order[static_cast<size_t>(bm) * p.Tc + rank];
+  const int ntiles = p.col_count[static_cast<size_t>(bm) * p.Tc + kb];
+  const int32_t* list = p.col_list + (static_cast<size_t>(bm) * p.Tc + kb) * p.Tr;
+  const int head_row0 = bh * p.N;
+  const int k_row0 = head_row0 + kb * kTile;
+
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (tid == 0) record_failure(p.status, kStatusLayout, kSiteBwdSmemAlign);
+    return;
+  }
+  const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV),
+                 sDS = smem_u32(smem + L::kDS), sQ = smem_u32(smem + L::kQ),
+                 sDO = smem_u32(smem + L::kDO);
+  const float* lse_s = reinterpret_cast<const float*>(smem + L::kLse);
+  const float* delta_s = reinterpret_cast<const float*>(smem + L::kDelta);
+  const BwdBars bar{smem_u32(smem + L::kBar)};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(bar.kv_full(), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar.q_full(s), 1);
+      mbar_init(bar.q_empty(s), 1);
+    }
+    mbar_init(bar.s_full(), 1);
+    mbar_init(bar.dp_full(), 1);
+    mbar_init(bar.pt_ready(), 128);
+    mbar_init(bar.ds_ready(), 128);
+    mbar_init(bar.dv_done(), 1);
+    mbar_init(bar.tile_done(), 1);
+    mbar_init(bar.dq_drained(), 128);
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      tma_prefetch_desc(&mdo);
+      mbar_arrive_expect_tx(bar.kv_full(), 2 * L::kTileBytes);
+      for (int ch = 0; ch < L::kChunks; ++ch) {
+        tma_load_2d(sK + ch * 16384, &mk, ch * 64, k_row0, bar.kv_full());
+        tma_load_2d(sV + ch * 16384, &mv, ch * 64, k_row0, bar.kv_full());
+      }
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t & 1;
+        const int q_row = head_row0 + (list[t] >> 2) * kTile;
+        if (t >= 2 && !mbar_wait(bar.q_empty(st), ((t >> 1) - 1) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteBwdQEmpty);
+          break;
+        }
+        mbar_arrive_expect_tx(bar.q_full(st), 2 * L::kTileBytes + 2 * kTile * 4);
+        for (int ch = 0; ch < L::kChunks; ++ch) {
+          tma_load_2d(sQ + st * L::kTileBytes + ch * 16384, &mq, ch * 64, q_row, bar.q_full(st));
+          tma_load_2d(sDO + st * L::kTileBytes + ch * 16384, &mdo, ch * 64, q_row,
+                      bar.q_full(st));
+        }
+        bulk_load(smem_u32(lse_s + st * kTile), p.lse2 + q_row, kTile * 4, bar.q_full(st));
+        bulk_load(smem_u32(delta_s + st * kTile), p.delta + q_row, kTile * 4, bar.q_full(st));
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t id_st = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
+      constexpr uint32_t id_kd = idesc_bf16(128, D, 0, 1);    // dV, dK
+      constexpr uint32_t id_dq = idesc_bf16(128, D, 1, 1);    // dQ
+      bool ok = mbar_wait(bar.kv_full(), 0, p.status);
+      if (!ok) record_failure(p.status, kStatusTimeout, kSiteBwdKV);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int st = t & 1;
+        const uint32_t q = sQ + st * L::kTileBytes, g = sDO + st * L::kTileBytes;
+        if (!mbar_wait(bar.q_full(st), (t >> 1) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteBwdQ);
+          break;
+        }
+        if (t >= 1 && !mbar_wait(bar.dv_done(), (t - 1) & 1, p.status)) {  // P^T_{t-1} consumed
+          record_failure(p.status, kStatusTimeout, kSiteBwdDV);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q + off, 16, 1024),
+                 id_st, k > 0);
+        }
+        mma_commit(bar.s_full());
+        if (t >= 1 && !mbar_wait(bar.dq_drained(), (t - 1) & 1, p.status)) {  // dQ_{t-1} read out
+          record_failure(p.status, kStatusTimeout, kSiteBwdDrained);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(g + off, 16, 1024),
+                 id_st, k > 0);
+        }
+        mma_commit(bar.dp_full());
+        if (!mbar_wait(bar.pt_ready(), t & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteBwdPT);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + kColDV, tmem + kColS + k * 8, sdesc_sw128(g + k * 2048, 16384, 1024),
+                 id_kd, (t > 0 || k > 0));
+        mma_commit(bar.dv_done());
+        if (!mbar_wait(bar.ds_ready(), t & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteBwdDS);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tmem + kColDK, sdesc_sw128(sDS + off, 16, 1024),
+                 sdesc_sw128(q + k * 2048, 16384, 1024), id_kd, (t > 0 || k > 0));
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + kColDP, sdesc_sw128(sDS + k * 2048, 16384, 1024),
+                 sdesc_sw128(sK + k * 2048, 16384, 1024), id_dq, k > 0);
+        mma_commit(bar.tile_done());
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ compute (thread = key)
+    const int j = tid;
+    const int key = kb * kTile + j;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const size_t col = static_cast<size_t>(bm) * p.N + key;
+    const int lts = p.mask.lts[col], lte = p.mask.lte[col];
+    const int uts = p.mask.uts ? p.mask.uts[col] : 0, ute = p.mask.ute ? p.mask.ute[col] : 0;
+    const bool causal = p.mask.causal != 0;
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t & 1;
+      const int entry = list[t];
+      const int qb = entry >> 2, lab = entry & 3;
+      if (!mbar_wait(bar.q_full(st), (t >> 1) & 1, p.status) || !mbar_wait(bar.s_full(), t & 1, p.status)) {
+        record_failure(p.status, kStatusTimeout, kSiteBwdS);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float* ls = lse_s + st * kTile;
+      uint32_t pk[64];  // P^T row as bf16 pairs (the dV operand and the dS input)
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        // masked-query bits of this thread's key column for queries [32ch, 32ch+32)
+        const uint32_t mb = (lab == FM_TILE_PARTIAL)
+                                ? column_mask_bits(key, lts, lte, uts, ute, causal,
+                                                   qb * kTile + 32 * ch)
+                                : 0u;
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kColS + ch * 32, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float p0 = ex2(fmaf(__uint_as_float(v[2 * i]), c, -ls[ch * 32 + 2 * i]));
+          float p1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), c, -ls[ch * 32 + 2 * i + 1]));
+          p0 = ((mb >> (2 * i)) & 1u) ? 0.f : p0;
+          p1 = ((mb >> (2 * i + 1)) & 1u) ? 0.f : p1;
+          pk[ch * 16 + i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16p(tmem + lane_base + kColS + ch * 16, &pk[ch * 16]);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar.pt_ready());
+
+      if (!mbar_wait(bar.dp_full(), t & 1, p.status)) {
+        record_failure(p.status, kStatusTimeout, kSiteBwdDP);
+        ok = false;
+        break;
+      }
+      if (t >= 1 && !mbar_wait(bar.tile_done(), (t - 1) & 1, p.status)) {  // dS_{t-1} consumed
+        record_failure(p.status, kStatusTimeout, kSiteBwdDone);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float* dl = delta_s + st * kTile;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kColDP + ch * 32, v);
+        uint32_t dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int q0 = ch * 32 + 2 * i;
+          const uint32_t pw = pk[ch * 16 + i];
+          const float d0 = __uint_as_float(pw << 16) * (__uint_as_float(v[2 * i]) - dl[q0]);
+          const float d1 =
+              __uint_as_float(pw & 0xffff0000u) * (__uint_as_float(v[2 * i + 1]) - dl[q0 + 1]);
+          dk[i] = pack_bf16x2(d0, d1);
+        }
+        // row j of dS^T, queries [32ch, 32ch+32): four 16-byte pieces
+        const uint32_t base = sDS + (ch >> 1) * 16384;
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc)
+          st_shared_v4(base + sw128_offset(j, (ch & 1) * 4 + pc), dk[4 * pc], dk[4 * pc + 1],
+                       dk[4 * pc + 2], dk[4 * pc + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar.ds_ready());
+    }
+    // ------------------------------------------------------------ epilogue: dV, dK
+    if (ok && ntiles > 0) {
+      if (!mbar_wait(bar.tile_done(), (ntiles - 1) & 1, p.status)) {
+        record_failure(p.status, kStatusTimeout, kSiteBwdDone);
+        ok = false;
+      }
+      tc_fence_after();
+    }
+    const bool live = ok && ntiles > 0;
+    uint16_t* dv_row = p.dv + static_cast<size_t>(k_row0 + j) * D;
+    uint16_t* dk_row = p.dk + static_cast<size_t>(k_row0 + j) * D;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t colbase = which == 0 ? kColDV : kColDK;
+      const float f = which == 0 ? 1.f : p.scale;
+      uint16_t* dst_row = which == 0 ? dv_row : dk_row;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        if (live) {
+          tmem_ld32(tmem + lane_base + colbase + ch * 32, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        store_row32_bf16(dst_row + ch * 32, v, f);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain (thread = query)
+    // dQ_t (fp32, 128 queries x d) goes to the stage buffers of tile t in
+    // 32-column boxes of 128 rows x 128 bytes, 128-byte swizzled, then one
+    // thread adds the boxes into the global accumulator with TMA.
+    const int qq = tid - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool leader = tid == 128;
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t & 1;
+      const int qb = list[t] >> 2;
+      if (!mbar_wait(bar.tile_done(), t & 1, p.status)) {
+        record_failure(p.status, kStatusTimeout, kSiteBwdDQ);
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kColDP + ch * 32, v);
+        const uint32_t box = (ch * 16384 < L::kTileBytes)
+                                 ? sQ + st * L::kTileBytes + ch * 16384
+                                 : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16)
+          st_shared_v4(box + sw128_offset(qq, c16), v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2],
+                       v[4 * c16 + 3]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar.dq_drained());
+      fence_proxy_async_smem();
+      drain_bar();
+      if (leader) {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          const uint32_t box = (ch * 16384 < L::kTileBytes)
+                                   ? sQ + st * L::kTileBytes + ch * 16384
+                                   : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
+          tma_reduce_add_2d(&mdq, box, ch * 32, head_row0 + qb * kTile);
+        }
+        bulk_commit_group();
+        bulk_wait_read_all();  // the stage buffers may be refilled now
+        if (t + 2 < ntiles) mbar_arrive(bar.q_empty(st));
+      }
+    }
+    if (leader) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, float scale,
+                                                         uint16_t* __restrict__ dq,
+                                                         long long n8) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+  uint4 o;
+  o.x = pack_bf16x2(a.x * scale, a.y * scale);
+  o.y = pack_bf16x2(a.z * scale, a.w * scale);
+  o.z = pack_bf16x2(b.x * scale, b.y * scale);
+  o.w = pack_bf16x2(b.z * scale, b.w * scale);
+  reinterpret_cast<uint4*>(dq)[i] = o;
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
+                         cudaStream_t s) {
+  using L = BwdLayout<D>;
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       L::kBytes);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(p.B * p.H * p.Tc);
+  bwd_kernel<D><<<grid, 320, L::kBytes, s>>>(mq, mk, mv, mdo, mdq, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
+                           float* delta, float* lse2, float* dq_accum, long long rows,
+                           cudaStream_t s) {
+  const long long threads = rows * (d / 8);
+  const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
+  if (d == 64)
+    bwd_pre_kernel<64><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows);
+  else
+    bwd_pre_kernel<128><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
+                       cudaStream_t s) {
+  if (d == 64) return launch_bwd_t<64>(mq, mk, mv, mdo, mdq, p, s);
+  return launch_bwd_t<128>(mq, mk, mv, mdo, mdq, p, s);
+}
+
+cudaError_t launch_dq_convert(int d, const float* dq_accum, float scale, uint16_t* dq,
+                              long long elems, cudaStream_t s) {
+  (void)d;
+  const long long n8 = elems / 8;
+  const unsigned grid = static_cast<unsigned>((n8 + 255) / 256);
+  dq_convert_kernel<<<grid, 256, 0, s>>>(dq_accum, scale, dq, n8);
+  return cudaGetLastError();
+}
+
+}  // namespace fm

@@ -1,0 +1,352 @@
+// Host side of the C ABI declared in include/flashmask.h: argument checks,
+// workspace layout, TMA descriptors and kernel launches. Nothing here
+// allocates device memory.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "../../include/flashmask.h"
+
+namespace {
+
+using fm::kTile;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool shape_ok(int B, int H, int Hm, int N, int d) {
+  if (B <= 0 || H <= 0 || Hm <= 0 || N <= 0) return false;
+  if (d != 64 && d != 128) return false;
+  if (N % kTile != 0) return false;
+  if (H % Hm != 0) return false;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows >= (1LL << 31)) return false;
+  return true;
+}
+
+fm_ws_layout make_layout(int B, int H, int Hm, int N, int d, int for_bwd) {
+  fm_ws_layout L;
+  std::memset(&L, 0, sizeof(L));
+  const size_t Tr = N / kTile, Tc = Tr, BHm = static_cast<size_t>(B) * Hm;
+  const size_t BHN = static_cast<size_t>(B) * H * N;
+  size_t off = 0;
+  L.status = off;
+  off = align_up(off + 16, 256);
+  L.minmax = off;
+  off = align_up(off + BHm * Tc * 8 * 4, 256);
+  L.labels = off;
+  off = align_up(off + BHm * Tr * Tc, 256);
+  L.labels_t = off;
+  off = align_up(off + BHm * Tc * Tr, 256);
+  L.row_count = off;
+  off = align_up(off + BHm * Tr * 4, 256);
+  L.row_list = off;
+  off = align_up(off + BHm * Tr * Tc * 4, 256);
+  L.row_order = off;
+  off = align_up(off + BHm * Tr * 4, 256);
+  L.col_count = off;
+  off = align_up(off + BHm * Tc * 4, 256);
+  L.col_list = off;
+  off = align_up(off + BHm * Tc * Tr * 4, 256);
+  L.col_order = off;
+  off = align_up(off + BHm * Tc * 4, 256);
+  if (for_bwd) {
+    L.lse2 = off;
+    off = align_up(off + BHN * 4, 256);
+    L.delta = off;
+    off = align_up(off + BHN * 4, 256);
+    L.dq_accum = off;
+    off = align_up(off + BHN * d * 4, 256);
+  }
+  L.total = off;
+  return L;
+}
+
+fm::ClassifyTables tables(const fm_ws_layout& L, void* ws) {
+  char* w = static_cast<char*>(ws);
+  fm::ClassifyTables t;
+  t.minmax = reinterpret_cast<int32_t*>(w + L.minmax);
+  t.labels = reinterpret_cast<uint8_t*>(w + L.labels);
+  t.labels_t = reinterpret_cast<uint8_t*>(w + L.labels_t);
+  t.row_count = reinterpret_cast<int32_t*>(w + L.row_count);
+  t.row_list = reinterpret_cast<int32_t*>(w + L.row_list);
+  t.row_order = reinterpret_cast<int32_t*>(w + L.row_order);
+  t.col_count = reinterpret_cast<int32_t*>(w + L.col_count);
+  t.col_list = reinterpret_cast<int32_t*>(w + L.col_list);
+  t.col_order = reinterpret_cast<int32_t*>(w + L.col_order);
+  return t;
+}
+
+bool mask_ok(const fm_mask* m) {
+  if (!m || !m->lts || !m->lte) return false;
+  if ((m->uts == nullptr) != (m->ute == nullptr)) return false;
+  return true;
+}
+
+fm::MaskDev mask_dev(const fm_mask* m) {
+  fm::MaskDev d;
+  d.lts = m->lts;
+  d.lte = m->lte;
+  d.uts = m->uts;
+  d.ute = m->ute;
+  d.Hm = m->Hm;
+  d.causal = m->causal ? 1 : 0;
+  return d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Tensor map over the [rows, d] fp32 dQ accumulator with 128-row x 32-column
+// boxes (128 bytes wide) and 128-byte swizzle, used for TMA reduce-add.
+bool make_map_f32(CUtensorMap* m, const void* base, long long rows, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map over a [rows, d] bf16 matrix with 128-row x 64-column boxes and
+// 128-byte swizzle (the layout the tcgen05 descriptors expect).
+bool make_map(CUtensorMap* m, const void* base, long long rows, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+fm_status check_ws(void* ws, size_t ws_bytes, const fm_ws_layout& L) {
+  if (!ws) return FM_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FM_ERR_WORKSPACE;
+  if (ws_bytes < L.total) return FM_ERR_WORKSPACE;
+  return FM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t flashmask_workspace_bytes(int B, int H, int Hm, int N, int d, int for_bwd) {
+  if (!shape_ok(B, H, Hm, N, d)) return 0;
+  return make_layout(B, H, Hm, N, d, for_bwd).total;
+}
+
+fm_status flashmask_workspace_layout(int B, int H, int Hm, int N, int d, int for_bwd,
+                                     fm_ws_layout* out) {
+  if (!out) return FM_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, Hm, N, d)) return FM_ERR_UNSUPPORTED;
+  *out = make_layout(B, H, Hm, N, d, for_bwd);
+  return FM_OK;
+}
+
+fm_status flashmask_classify(const fm_mask* mask, int B, int N, void* ws, size_t ws_bytes,
+                             void* stream) {
+  if (!mask_ok(mask)) return FM_ERR_INVALID_ARG;
+  const int Hm = mask->Hm;
+  // the classification part of the layout depends on (B, Hm, N) only
+  if (!shape_ok(B, Hm, Hm, N, 64)) return FM_ERR_UNSUPPORTED;
+  const fm_ws_layout L = make_layout(B, Hm, Hm, N, 64, 0);
+  const fm_status ws_st = check_ws(ws, ws_bytes, L);
+  if (ws_st != FM_OK) return ws_st;
+  cudaError_t e = fm::launch_classify(mask_dev(mask), B, N, tables(L, ws),
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_mask* mask, int B,
+                        int H, int N, int d, float scale, void* o, float* lse, void* ws,
+                        size_t ws_bytes, int ws_classified, void* stream) {
+  if (!q || !k || !v || !o || !lse || !mask_ok(mask)) return FM_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, mask->Hm, N, d)) return FM_ERR_UNSUPPORTED;
+  const fm_ws_layout L = make_layout(B, H, mask->Hm, N, d, 0);
+  const fm_status ws_st = check_ws(ws, ws_bytes, L);
+  if (ws_st != FM_OK) return ws_st;
+  const long long rows = static_cast<long long>(B) * H * N;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, rows, d) || !make_map(&mk, k, rows, d) || !make_map(&mv, v, rows, d))
+    return FM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const fm::ClassifyTables t = tables(L, ws);
+  if (!ws_classified) {
+    if (fm::launch_classify(mask_dev(mask), B, N, t, s) != cudaSuccess) return FM_ERR_CUDA;
+  }
+  fm::FwdParams p;
+  p.mask = mask_dev(mask);
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.Tr = N / kTile;
+  p.Tc = N / kTile;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.row_count = t.row_count;
+  p.row_list = t.row_list;
+  p.row_order = t.row_order;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.status = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.status);
+  return fm::launch_fwd(d, mq, mk, mv, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status flashmask_bwd_preprocess(const void* o, const float* lse, const void* dout, int B, int H,
+                                   int Hm, int N, int d, void* ws, size_t ws_bytes, void* stream) {
+  if (!o || !lse || !dout) return FM_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(lse)) return FM_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, Hm, N, d)) return FM_ERR_UNSUPPORTED;
+  const fm_ws_layout L = make_layout(B, H, Hm, N, d, 1);
+  const fm_status ws_st = check_ws(ws, ws_bytes, L);
+  if (ws_st != FM_OK) return ws_st;
+  char* w = static_cast<char*>(ws);
+  const long long rows = static_cast<long long>(B) * H * N;
+  return fm::launch_bwd_pre(d, static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
+                            lse, reinterpret_cast<float*>(w + L.delta),
+                            reinterpret_cast<float*>(w + L.lse2),
+                            reinterpret_cast<float*>(w + L.dq_accum), rows,
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FM_OK
+             : FM_ERR_CUDA;
+}
+
+fm_status flashmask_bwd_main(const void* q, const void* k, const void* v, const void* dout,
+                             const fm_mask* mask, int B, int H, int N, int d, float scale,
+                             void* dk, void* dv, void* ws, size_t ws_bytes, void* stream) {
+  if (!q || !k || !v || !dout || !dk || !dv || !mask_ok(mask)) return FM_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dk) ||
+      !aligned16(dv))
+    return FM_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, mask->Hm, N, d)) return FM_ERR_UNSUPPORTED;
+  const fm_ws_layout L = make_layout(B, H, mask->Hm, N, d, 1);
+  const fm_status ws_st = check_ws(ws, ws_bytes, L);
+  if (ws_st != FM_OK) return ws_st;
+  const long long rows = static_cast<long long>(B) * H * N;
+  char* w = static_cast<char*>(ws);
+  float* dq_accum = reinterpret_cast<float*>(w + L.dq_accum);
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  if (!make_map(&mq, q, rows, d) || !make_map(&mk, k, rows, d) || !make_map(&mv, v, rows, d) ||
+      !make_map(&mdo, dout, rows, d) || !make_map_f32(&mdq, dq_accum, rows, d))
+    return FM_ERR_CUDA;
+  const fm::ClassifyTables t = tables(L, ws);
+  fm::BwdParams p;
+  p.mask = mask_dev(mask);
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.Tr = N / kTile;
+  p.Tc = N / kTile;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.col_count = t.col_count;
+  p.col_list = t.col_list;
+  p.col_order = t.col_order;
+  p.lse2 = reinterpret_cast<float*>(w + L.lse2);
+  p.delta = reinterpret_cast<float*>(w + L.delta);
+  p.dq_accum = dq_accum;
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
+  p.status = reinterpret_cast<int32_t*>(w + L.status);
+  return fm::launch_bwd(d, mq, mk, mv, mdo, mdq, p, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FM_OK
+             : FM_ERR_CUDA;
+}
+
+fm_status flashmask_bwd_finalize(int B, int H, int Hm, int N, int d, float scale, void* dq,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  if (!dq || !aligned16(dq)) return FM_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FM_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, Hm, N, d)) return FM_ERR_UNSUPPORTED;
+  const fm_ws_layout L = make_layout(B, H, Hm, N, d, 1);
+  const fm_status ws_st = check_ws(ws, ws_bytes, L);
+  if (ws_st != FM_OK) return ws_st;
+  const long long elems = static_cast<long long>(B) * H * N * d;
+  return fm::launch_dq_convert(d, reinterpret_cast<const float*>(static_cast<char*>(ws) + L.dq_accum),
+                               scale, static_cast<uint16_t*>(dq), elems,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FM_OK
+             : FM_ERR_CUDA;
+}
+
+fm_status flashmask_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dout, const fm_mask* mask, int B, int H,
+                        int N, int d, float scale, void* dq, void* dk, void* dv, void* ws,
+                        size_t ws_bytes, int ws_classified, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !mask_ok(mask))
+    return FM_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse))
+    return FM_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, mask->Hm, N, d)) return FM_ERR_UNSUPPORTED;
+  const fm_ws_layout L = make_layout(B, H, mask->Hm, N, d, 1);
+  const fm_status ws_st = check_ws(ws, ws_bytes, L);
+  if (ws_st != FM_OK) return ws_st;
+  if (!ws_classified) {
+    if (fm::launch_classify(mask_dev(mask), B, N, tables(L, ws), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+      return FM_ERR_CUDA;
+  }
+  fm_status st = flashmask_bwd_preprocess(o, lse, dout, B, H, mask->Hm, N, d, ws, ws_bytes, stream);
+  if (st != FM_OK) return st;
+  st = flashmask_bwd_main(q, k, v, dout, mask, B, H, N, d, scale, dk, dv, ws, ws_bytes, stream);
+  if (st != FM_OK) return st;
+  return flashmask_bwd_finalize(B, H, mask->Hm, N, d, scale, dq, ws, ws_bytes, stream);
+}
+
+fm_status flashmask_check_status(void* ws, void* stream, int* detail) {
+  if (detail) *detail = 0;
+  if (!ws) return FM_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FM_ERR_CUDA;
+  int32_t h[2] = {0, 0};
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FM_ERR_CUDA;
+  if (h[0] == 0) return FM_OK;
+  if (detail) *detail = h[1];
+  if (cudaMemset(ws, 0, sizeof(h)) != cudaSuccess) return FM_ERR_CUDA;
+  return FM_ERR_TIMEOUT;
+}
+
+const char* flashmask_status_string(fm_status s) {
+  switch (s) {
+    case FM_OK: return "ok";
+    case FM_ERR_INVALID_ARG: return "invalid argument";
+    case FM_ERR_UNSUPPORTED: return "unsupported shape";
+    case FM_ERR_CUDA: return "CUDA error";
+    case FM_ERR_TIMEOUT: return "a kernel wait timed out";
+    case FM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

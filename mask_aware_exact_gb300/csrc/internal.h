@@ -1,0 +1,85 @@
+// Host-side launch interface shared by the C ABI and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fm {
+
+constexpr int kTile = 128;
+
+// Device status word layout (int32[4] at the start of the workspace):
+//   [0] bit mask of failures (kStatusTimeout, kStatusLayout)
+//   [1] first failure site (one of the Site codes below), 0 if none
+enum : int { kStatusTimeout = 1, kStatusLayout = 2 };
+enum Site : int {
+  kSiteNone = 0,
+  kSiteFwdQ = 101, kSiteFwdK, kSiteFwdV, kSiteFwdS, kSiteFwdP, kSiteFwdO, kSiteFwdKEmpty,
+  kSiteFwdVEmpty, kSiteFwdSmemAlign,
+  kSiteBwdKV = 201, kSiteBwdQ, kSiteBwdQEmpty, kSiteBwdS, kSiteBwdDP, kSiteBwdPT, kSiteBwdDS,
+  kSiteBwdDV, kSiteBwdDQ, kSiteBwdDrained, kSiteBwdDone, kSiteBwdSmemAlign,
+};
+
+struct MaskDev {
+  const int32_t* lts;
+  const int32_t* lte;
+  const int32_t* uts;  // may be null (then ute is null too)
+  const int32_t* ute;
+  int Hm;
+  int causal;
+};
+
+struct ClassifyTables {
+  int32_t* minmax;     // [B,Hm,Tc,8]
+  uint8_t* labels;     // [B,Hm,Tr,Tc]
+  uint8_t* labels_t;   // [B,Hm,Tc,Tr]
+  int32_t* row_count;  // [B,Hm,Tr]
+  int32_t* row_list;   // [B,Hm,Tr,Tc]
+  int32_t* row_order;  // [B,Hm,Tr]
+  int32_t* col_count;  // [B,Hm,Tc]
+  int32_t* col_list;   // [B,Hm,Tc,Tr]
+  int32_t* col_order;  // [B,Hm,Tc]
+};
+
+struct FwdParams {
+  MaskDev mask;
+  int B, H, N, Tr, Tc;
+  float scale_log2;  // scale * log2(e)
+  const int32_t* row_count;
+  const int32_t* row_list;
+  const int32_t* row_order;
+  uint16_t* o;  // bf16 [B,H,N,d]
+  float* lse;   // [B,H,N]
+  int32_t* status;
+};
+
+struct BwdParams {
+  MaskDev mask;
+  int B, H, N, Tr, Tc;
+  float scale;       // applied to dK here and to dQ in the conversion kernel
+  float scale_log2;  // scale * log2(e)
+  const int32_t* col_count;
+  const int32_t* col_list;
+  const int32_t* col_order;
+  const float* lse2;   // [B,H,N]
+  const float* delta;  // [B,H,N]
+  float* dq_accum;     // [B,H,N,d]
+  uint16_t* dk;
+  uint16_t* dv;
+  int32_t* status;
+};
+
+cudaError_t launch_classify(const MaskDev& m, int B, int N, const ClassifyTables& t,
+                            cudaStream_t s);
+cudaError_t launch_fwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const FwdParams& p, cudaStream_t s);
+cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
+                           float* delta, float* lse2, float* dq_accum, long long rows,
+                           cudaStream_t s);
+cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
+                       cudaStream_t s);
+cudaError_t launch_dq_convert(int d, const float* dq_accum, float scale, uint16_t* dq,
+                              long long elems, cudaStream_t s);
+
+}  // namespace fm

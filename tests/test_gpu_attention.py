@@ -1,0 +1,184 @@
+"""CUDA forward and backward vs the fp64 oracle, element by element.
+
+Small cases are compared in full (several tiles, PARTIAL and NONE tiles, fully
+masked rows, mask heads, d = 64 and 128). The large workloads run in the same
+launch configuration the benchmark times and are compared on sampled outputs
+that the oracle computes one by one: query rows for O, LSE and dQ; key blocks
+for dK and dV, using exactly the query rows that can see those keys (rows that
+cannot see key j contribute nothing to dK_j or dV_j)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from mask_aware_exact_gb300 import workloads as W
+from oracle import attention as A
+
+from gpu_common import (check_forward, check_grad, head_bounds, need_gpu, run_path, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def full_compare(fm, q, k, v, do, spec, scale=None, what=""):
+    B, H, N, d = q.shape
+    scale_v = 1 / math.sqrt(d) if scale is None else scale
+    out = run_path(fm, q, k, v, do, spec, scale=scale)
+    o_ref, lse_ref = A.forward(q, k, v, spec, scale_v)
+    dq_ref, dk_ref, dv_ref = A.backward(q, k, v, do, spec, scale_v)
+    check_forward(to_np(out["o"]), to_np(out["lse"]), o_ref, lse_ref, what)
+    check_grad("Q", to_np(out["dq"]), dq_ref, what)
+    check_grad("K", to_np(out["dk"]), dk_ref, what)
+    check_grad("V", to_np(out["dv"]), dv_ref, what)
+    return out
+
+
+def test_document_small_workload_full():
+    fm = need_gpu()
+    w = W.workload(0)
+    q, k, v, do = W.make_qkv(w.B, w.H, w.N, w.d, w.seed)
+    full_compare(fm, q, k, v, do, w.mask, what=w.name)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("kind", ["causal", "document", "window_prefix", "share_question",
+                                  "unmasked"])
+def test_families_small(kind, d):
+    fm = need_gpu()
+    B, H, N = 2, 2, 640  # 5 x 5 tiles
+    if kind == "causal":
+        spec = W.causal_bounds(B, 1, N)
+    elif kind == "document":
+        spec = W.document_bounds(B, 1, [200, 37, 300, 103])
+    elif kind == "window_prefix":
+        spec = W.window_prefix_bounds(B, 1, N, 160, 96)
+    elif kind == "share_question":
+        spec = W.share_question_bounds(B, 1, 192, [150, 170, 128])
+    else:
+        e = np.full((B, 1, N), N, np.int32)
+        spec = W.MaskSpec("none", False, e, e.copy(), None, None)
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=7)
+    full_compare(fm, q, k, v, do, spec, what=f"{kind} d={d}")
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_bounds_with_fully_masked_rows(seed):
+    fm = need_gpu()
+    B, H, N, d = 1, 4, 384, 128
+    Hm = [1, 2, 4, 1][seed]
+    spec = W.random_bounds(B, Hm, N, causal=seed % 2 == 0, seed=300 + seed, upper=True)
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=seed)
+    full_compare(fm, q, k, v, do, spec, what=f"random seed {seed}")
+
+
+def test_fully_masked_rows_inside_partial_tiles():
+    # rows 64..99 and 300..301 see no key at all; their tiles also hold
+    # visible rows, so the convention is exercised inside PARTIAL tiles
+    fm = need_gpu()
+    B, H, N, d = 1, 2, 384, 128
+    lts = np.full((1, 1, N), 64, np.int32)
+    lte = np.full((1, 1, N), 100, np.int32)
+    uts = np.full((1, 1, N), 300, np.int32)
+    ute = np.full((1, 1, N), 302, np.int32)
+    spec = W.MaskSpec("holes", True, lts, lte, uts, ute)
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=21)
+    out = full_compare(fm, q, k, v, do, spec, what="masked rows")
+    lse = to_np(out["lse"])
+    assert np.all(np.isneginf(lse[:, :, 64:100])) and np.all(np.isneginf(lse[:, :, 300:302]))
+    assert np.isfinite(lse[:, :, :64]).all() and np.isfinite(lse[:, :, 100:300]).all()
+
+
+def test_all_masked_and_all_visible_blocks():
+    # query block 1 entirely masked (every tile FULL), block 0 entirely visible
+    fm = need_gpu()
+    B, H, N, d = 1, 2, 256, 64
+    lts = np.full((1, 1, N), 128, np.int32)
+    lte = np.full((1, 1, N), 256, np.int32)
+    spec = W.MaskSpec("block", False, lts, lte, None, None)
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=11)
+    out = full_compare(fm, q, k, v, do, spec, what="masked block")
+    assert np.all(np.isneginf(to_np(out["lse"])[:, :, 128:]))
+    assert np.all(to_np(out["dq"])[:, :, 128:] == 0)
+
+
+def test_custom_scale():
+    fm = need_gpu()
+    w = W.workload(0)
+    q, k, v, do = W.make_qkv(w.B, w.H, w.N, w.d, 3)
+    full_compare(fm, q, k, v, do, w.mask, scale=0.05, what="scale 0.05")
+
+
+def test_repeatable():
+    # forward and dK / dV are deterministic; dQ is summed by reductions whose
+    # order may vary, so it is only required within tolerance
+    fm = need_gpu()
+    B, H, N, d = 1, 4, 1024, 128
+    spec = W.document_bounds(B, 1, [300, 500, 224])
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=5)
+    a = run_path(fm, q, k, v, do, spec)
+    b = run_path(fm, q, k, v, do, spec)
+    for key in ("o", "lse", "dk", "dv"):
+        assert torch.equal(a[key], b[key]), key
+    assert (a["dq"].float() - b["dq"].float()).abs().max().item() < 1e-2
+
+
+# ---------------------------------------------------------------- full-size workloads
+def sampled_compare(w, out, q, k, v, do, heads, row_blocks, key_blocks):
+    d = w.d
+    scale = 1 / math.sqrt(d)
+    N = w.N
+    for (b, h) in heads:
+        lts, lte, uts, ute = head_bounds(w.mask, b, h, w.H)
+        causal = w.mask.causal
+        rows = np.concatenate([np.arange(r * 128, r * 128 + 128) for r in row_blocks])
+        o_ref, lse_ref = A.forward_head(q[b, h], k[b, h], v[b, h], lts, lte, uts, ute, causal,
+                                        scale, rows=rows)
+        check_forward(to_np(out["o"][b, h])[rows], to_np(out["lse"][b, h])[rows], o_ref, lse_ref,
+                      f"{w.name} head {(b, h)}")
+        dq_ref, _, _ = A.backward_head(q[b, h], k[b, h], v[b, h], do[b, h], lts, lte, uts, ute,
+                                       causal, scale, rows=rows)
+        check_grad("Q", to_np(out["dq"][b, h])[rows], dq_ref, f"{w.name} head {(b, h)}")
+        keys = np.concatenate([np.arange(c * 128, c * 128 + 128) for c in key_blocks])
+        # every query row that sees at least one sampled key
+        seen = np.zeros(N, bool)
+        for s in range(0, N, 2048):
+            vis = A.visible(np.arange(s, min(s + 2048, N)), N, lts, lte, uts, ute, causal)
+            seen[s:s + vis.shape[0]] = vis[:, keys].any(axis=1)
+        sub = np.nonzero(seen)[0]
+        _, dk_ref, dv_ref = A.backward_head(q[b, h], k[b, h], v[b, h], do[b, h], lts, lte, uts,
+                                            ute, causal, scale, rows=sub)
+        check_grad("K", to_np(out["dk"][b, h])[keys], dk_ref[keys], f"{w.name} head {(b, h)}")
+        check_grad("V", to_np(out["dv"][b, h])[keys], dv_ref[keys], f"{w.name} head {(b, h)}")
+
+
+SAMPLES = {
+    # workload index: (heads, query blocks, key blocks)
+    1: ([(0, 0), (3, 15)], [0, 31, 63], [0, 40, 63]),
+    2: ([(0, 0), (0, 31)], [0, 55, 56, 200, 255], [3, 60, 180, 255]),
+    3: ([(0, 0), (1, 31)], [0, 31, 40, 90, 127], [5, 33, 64, 120]),
+    4: ([(0, 0), (0, 7)], [0, 15, 16, 17, 500, 1023], [16, 17, 400, 1023]),
+}
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4])
+def test_full_size_workload_sampled(idx):
+    fm = need_gpu()
+    w = W.workload(idx)
+    q, k, v, do = W.make_qkv(w.B, w.H, w.N, w.d, w.seed)
+    out = run_path(fm, q, k, v, do, w.mask)
+    heads, rb, kb = SAMPLES[idx]
+    sampled_compare(w, out, q, k, v, do, heads, rb, kb)
+    # properties that hold at any size: finite outputs, every row sees a key
+    for key in ("o", "dq", "dk", "dv"):
+        assert torch.isfinite(out[key].float()).all(), key
+    assert torch.isfinite(out["lse"]).all()
+
+
+def test_window_prefix_reduced_full():
+    # the prefix columns of the 128K window workload are seen by every row, so
+    # their dK / dV are checked in full on the same family at N = 8192
+    fm = need_gpu()
+    B, H, N, d = 1, 2, 8192, 128
+    spec = W.window_prefix_bounds(B, 1, N, 4096, 2048)
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=0)
+    full_compare(fm, q, k, v, do, spec, what="window_prefix N=8192")
