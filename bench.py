@@ -62,11 +62,13 @@ def kernel_source_hash(files=("bwd.cu", "ptx.cuh")) -> str:
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons with nvidia-smi every 50 ms; stop()
+    summarises the samples whose timestamps fall inside [t_begin, t_end]."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -77,7 +79,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -88,32 +90,47 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self) -> dict:
+    @staticmethod
+    def _ts(text: str) -> float:
+        from datetime import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return float("nan")
+
+    def stop(self, t_begin: float, t_end: float) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
         self.proc.terminate()
         try:
             self.proc.wait(5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(2)
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, power, reasons, n_all = [], [], [], set(), 0
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
+                continue
+            n_all += 1
+            ts = self._ts(parts[0])
+            if not (t_begin - 0.05 <= ts <= t_end + 0.05):
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+                power.append(float(parts[4]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(self.NAMES, parts[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None,
+                    "reasons": [f"no samples inside the timed region ({n_all} outside)"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
 
@@ -173,6 +190,8 @@ def run_native(args):
         if ev is not None:
             ev[5].record(stream)
 
+    clocks = ClockSampler(local)
+    clocks.start()
     for _ in range(args.warmup):
         step()
     st, site = fm.flashmask_check_status(ws)
@@ -182,17 +201,17 @@ def run_native(args):
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
-    clocks.start()
     R.barrier()
     torch.cuda.synchronize()
+    wall0 = time.time()
     t0.record(stream)
     for i in range(K):
         step(evs[i])
     t1.record(stream)
     torch.cuda.synchronize()
+    wall1 = time.time()
     R.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(wall0, wall1)
     elapsed_s = t0.elapsed_time(t1) / 1e3
     st, site = fm.flashmask_check_status(ws)
     if st != fm.FM_OK:
@@ -377,8 +396,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", type=int, default=2, help="synthetic workload index 0..4")
     ap.add_argument("--no-cpu-baseline", action="store_true")

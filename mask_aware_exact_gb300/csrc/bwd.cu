@@ -13,27 +13,35 @@
 //                 dV  += P^T dO             (A from TMEM)
 //                 dS^T = P^T (dP^T - D)     -> bf16 in shared memory
 //                 dK  += dS^T Q             (dS^T K-major)
-//                 dQ_t = dS K               (dS^T read MN-major) -> TMEM
-//               dQ_t leaves TMEM through the tile's own Q/dO stage buffers (free
-//               once its MMAs are done) and a TMA bulk reduce-add into the
-//               global fp32 accumulator.
+//                 dQ_t                      -> TMEM -> fp32 global accumulator
+//               d = 128: dQ_t^T = K^T dS^T (M = d), one head dimension per TMEM
+//               lane, reduced from registers with coalesced fp32 adds.
+//               d = 64: dQ_t = dS K (M = queries), through the tile's own Q/dO
+//               stage buffers and a TMA bulk reduce-add.
 //   dq_convert  dQ = bf16(scale * accumulator).
 //
-// Warp roles of bwd_kernel: warps 0-3 compute (thread t = key t = TMEM lane t),
-// warps 4-7 drain dQ_t (thread t = query t), warp 8 TMA producer, warp 9 MMA
-// issuer.
+// Warp roles of bwd_kernel (448 threads): warps 0-7 compute, two warpgroups;
+// warpgroup g handles queries [64g, 64g+64) of every tile and thread (g, t)
+// owns key t (= TMEM lane t). Warps 8-11 drain dQ_t (thread t = query t),
+// warp 12 is the TMA producer, warp 13 the MMA issuer.
 //
 // TMEM columns (512): S^T / P^T [0,128)  dP^T / dQ_t [128,256)
 //                     dV [256, 256+d)    dK [384, 384+d)
+// Warpgroup g writes its bf16 P^T half into S^T columns [64g, 64g+32), which
+// only it has read, so the two warpgroups never race on TMEM.
 #include "internal.h"
 #include "ptx.cuh"
-#include "../../include/flashmask.h"
+#include "flashmask.h"
 
 namespace fm {
 
 namespace {
 
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+constexpr int kThreads = 448;
+
+// TMEM column of the P^T operand for queries [16k, 16k+16) (A of the dV MMA).
+__device__ __forceinline__ uint32_t pt_col(int k) { return kColS + 8 * k + (k >= 4 ? 32 : 0); }
 
 template <int D>
 struct BwdLayout {
@@ -97,6 +105,9 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -155,11 +166,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 
 // ---------------------------------------------------------------- main
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                const __grid_constant__ CUtensorMap mdq, const BwdParams p) {
   using L = BwdLayout<D>;
+  // d = 128: dQ^T lives in TMEM with one head dimension per lane and is reduced
+  // into the accumulator straight from registers (coalesced rows). d = 64: dQ
+  // (one query per lane) goes out through the stage buffers and a TMA reduce.
+  constexpr bool kDqT = (D == 128);
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -185,7 +200,7 @@ __global__ void __launch_bounds__(320, 1)
   const BwdBars bar{smem_u32(smem + L::kBar)};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -197,11 +212,11 @@ __global__ void __launch_bounds__(320, 1)
     }
     mbar_init(bar.s_full(), 1);
     mbar_init(bar.dp_full(), 1);
-    mbar_init(bar.pt_ready(), 128);
-    mbar_init(bar.ds_ready(), 128);
+    mbar_init(bar.pt_ready(), 8);
+    mbar_init(bar.ds_ready(), 8);
     mbar_init(bar.dv_done(), 1);
     mbar_init(bar.tile_done(), 1);
-    mbar_init(bar.dq_drained(), 128);
+    mbar_init(bar.dq_drained(), 4);
     fence_barrier_init();
   }
   tc_fence_before();
@@ -209,7 +224,7 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
       tma_prefetch_desc(&mq);
@@ -238,12 +253,13 @@ __global__ void __launch_bounds__(320, 1)
         bulk_load(smem_u32(delta_s + st * kTile), p.delta + q_row, kTile * 4, bar.q_full(st));
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t id_st = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t id_kd = idesc_bf16(128, D, 0, 1);    // dV, dK
-      constexpr uint32_t id_dq = idesc_bf16(128, D, 1, 1);    // dQ
+      constexpr uint32_t id_dq = kDqT ? idesc_bf16(128, 128, 1, 1)   // dQ^T (M = d = 128)
+                                      : idesc_bf16(128, D, 1, 1);    // dQ (M = queries)
       bool ok = mbar_wait(bar.kv_full(), 0, p.status);
       if (!ok) record_failure(p.status, kStatusTimeout, kSiteBwdKV);
       for (int t = 0; ok && t < ntiles; ++t) {
@@ -284,7 +300,7 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + kColDV, tmem + kColS + k * 8, sdesc_sw128(g + k * 2048, 16384, 1024),
+          mma_ts(tmem + kColDV, tmem + pt_col(k), sdesc_sw128(g + k * 2048, 16384, 1024),
                  id_kd, (t > 0 || k > 0));
         mma_commit(bar.dv_done());
         if (!mbar_wait(bar.ds_ready(), t & 1, p.status)) {
@@ -298,58 +314,85 @@ __global__ void __launch_bounds__(320, 1)
           mma_ss(tmem + kColDK, sdesc_sw128(sDS + off, 16, 1024),
                  sdesc_sw128(q + k * 2048, 16384, 1024), id_kd, (t > 0 || k > 0));
         }
+        if constexpr (kDqT) {
+          // dQ_t^T = K^T dS^T: A = the K tile read MN-major (M = d), B = dS^T read
+          // MN-major (N = queries); rows of the result are head dimensions
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + kColDP, sdesc_sw128(sDS + k * 2048, 16384, 1024),
-                 sdesc_sw128(sK + k * 2048, 16384, 1024), id_dq, k > 0);
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + kColDP, sdesc_sw128(sK + k * 2048, 16384, 1024),
+                   sdesc_sw128(sDS + k * 2048, 16384, 1024), id_dq, k > 0);
+        } else {
+          // dQ_t = dS K: A = dS^T read MN-major (M = queries), B = K read MN-major
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ss(tmem + kColDP, sdesc_sw128(sDS + k * 2048, 16384, 1024),
+                   sdesc_sw128(sK + k * 2048, 16384, 1024), id_dq, k > 0);
+        }
         mma_commit(bar.tile_done());
+        // Q_t and dO_t are no longer read; with dQ^T drained from registers the
+        // stage goes back to the producer at once
+        if (kDqT && t + 2 < ntiles) mma_commit(bar.q_empty(st));
       }
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ compute (thread = key)
-    const int j = tid;
+    const int g = warp >> 2;               // queries [64g, 64g+64) of each tile
+    const int j = (warp & 3) * 32 + lane;  // key within the block = TMEM lane
     const int key = kb * kTile + j;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const size_t col = static_cast<size_t>(bm) * p.N + key;
     const int lts = p.mask.lts[col], lte = p.mask.lte[col];
     const int uts = p.mask.uts ? p.mask.uts[col] : 0, ute = p.mask.ute ? p.mask.ute[col] : 0;
     const bool causal = p.mask.causal != 0;
     const float c = p.scale_log2;
     bool ok = true;
+    int next_entry = ntiles > 0 ? list[0] : 0;  // read one tile ahead
     for (int t = 0; t < ntiles; ++t) {
       const int st = t & 1;
-      const int entry = list[t];
+      const int entry = next_entry;
+      if (t + 1 < ntiles) next_entry = list[t + 1];
       const int qb = entry >> 2, lab = entry & 3;
-      if (!mbar_wait(bar.q_full(st), (t >> 1) & 1, p.status) || !mbar_wait(bar.s_full(), t & 1, p.status)) {
+      if (!mbar_wait(bar.q_full(st), (t >> 1) & 1, p.status) ||
+          !mbar_wait(bar.s_full(), t & 1, p.status)) {
         record_failure(p.status, kStatusTimeout, kSiteBwdS);
         ok = false;
         break;
       }
       tc_fence_after();
-      const float* ls = lse_s + st * kTile;
-      uint32_t pk[64];  // P^T row as bf16 pairs (the dV operand and the dS input)
+      const float* ls = lse_s + st * kTile + 64 * g;
+      uint32_t pk[32];  // P^T half-row as bf16 pairs (the dV operand and the dS input)
+      {
+        uint32_t v[64];
+        const uint32_t a = tmem + lane_base + kColS + 64 * g;
+        tmem_ld64(a, a + 32, v);
+        // masked-query bits of this thread's key column for queries 64g + [32h, 32h+32)
+        uint32_t mb[2] = {0u, 0u};
+        if (lab == FM_TILE_PARTIAL) {
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        // masked-query bits of this thread's key column for queries [32ch, 32ch+32)
-        const uint32_t mb = (lab == FM_TILE_PARTIAL)
-                                ? column_mask_bits(key, lts, lte, uts, ute, causal,
-                                                   qb * kTile + 32 * ch)
-                                : 0u;
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kColS + ch * 32, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float p0 = ex2(fmaf(__uint_as_float(v[2 * i]), c, -ls[ch * 32 + 2 * i]));
-          float p1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), c, -ls[ch * 32 + 2 * i + 1]));
-          p0 = ((mb >> (2 * i)) & 1u) ? 0.f : p0;
-          p1 = ((mb >> (2 * i + 1)) & 1u) ? 0.f : p1;
-          pk[ch * 16 + i] = pack_bf16x2(p0, p1);
+          for (int hh = 0; hh < 2; ++hh)
+            mb[hh] = column_mask_bits(key, lts, lte, uts, ute, causal,
+                                      qb * kTile + 64 * g + 32 * hh);
         }
-        tmem_st16p(tmem + lane_base + kColS + ch * 16, &pk[ch * 16]);
+#pragma unroll
+        for (int i4 = 0; i4 < 16; ++i4) {
+          const float4 l4 = reinterpret_cast<const float4*>(ls)[i4];  // broadcast
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int q0 = 4 * i4 + 2 * u;
+            float p0 = ex2(fmaf(__uint_as_float(v[q0]), c, -lv[2 * u]));
+            float p1 = ex2(fmaf(__uint_as_float(v[q0 + 1]), c, -lv[2 * u + 1]));
+            p0 = ((mb[q0 >> 5] >> (q0 & 31)) & 1u) ? 0.f : p0;
+            p1 = ((mb[q0 >> 5] >> ((q0 + 1) & 31)) & 1u) ? 0.f : p1;
+            pk[2 * i4 + u] = pack_bf16x2(p0, p1);
+          }
+        }
       }
+      tmem_st32p(tmem + lane_base + kColS + 64 * g, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar.pt_ready());
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.pt_ready());
 
       if (!mbar_wait(bar.dp_full(), t & 1, p.status)) {
         record_failure(p.status, kStatusTimeout, kSiteBwdDP);
@@ -362,31 +405,38 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
-      const float* dl = delta_s + st * kTile;
+      const float* dl = delta_s + st * kTile + 64 * g;
+      // row j of dS^T, queries [64g, 64g+64): the 128-byte row of chunk g, in
+      // two 32-query halves
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int hh = 0; hh < 2; ++hh) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kColDP + ch * 32, v);
+        tmem_ld32(tmem + lane_base + kColDP + 64 * g + 32 * hh, v);
         uint32_t dk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int q0 = ch * 32 + 2 * i;
-          const uint32_t pw = pk[ch * 16 + i];
-          const float d0 = __uint_as_float(pw << 16) * (__uint_as_float(v[2 * i]) - dl[q0]);
-          const float d1 =
-              __uint_as_float(pw & 0xffff0000u) * (__uint_as_float(v[2 * i + 1]) - dl[q0 + 1]);
-          dk[i] = pack_bf16x2(d0, d1);
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 d4 = reinterpret_cast<const float4*>(dl + 32 * hh)[i4];  // broadcast
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int i = 2 * i4 + u;
+            const uint32_t pw = pk[16 * hh + i];
+            const float d0 = __uint_as_float(pw << 16) * (__uint_as_float(v[2 * i]) - dv4[2 * u]);
+            const float d1 = __uint_as_float(pw & 0xffff0000u) *
+                             (__uint_as_float(v[2 * i + 1]) - dv4[2 * u + 1]);
+            dk[i] = pack_bf16x2(d0, d1);
+          }
         }
-        // row j of dS^T, queries [32ch, 32ch+32): four 16-byte pieces
-        const uint32_t base = sDS + (ch >> 1) * 16384;
+        const uint32_t base = sDS + g * 16384;
 #pragma unroll
         for (int pc = 0; pc < 4; ++pc)
-          st_shared_v4(base + sw128_offset(j, (ch & 1) * 4 + pc), dk[4 * pc], dk[4 * pc + 1],
+          st_shared_v4(base + sw128_offset(j, 4 * hh + pc), dk[4 * pc], dk[4 * pc + 1],
                        dk[4 * pc + 2], dk[4 * pc + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar.ds_ready());
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.ds_ready());
     }
     // ------------------------------------------------------------ epilogue: dV, dK
     if (ok && ntiles > 0) {
@@ -397,15 +447,15 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
     }
     const bool live = ok && ntiles > 0;
-    uint16_t* dv_row = p.dv + static_cast<size_t>(k_row0 + j) * D;
-    uint16_t* dk_row = p.dk + static_cast<size_t>(k_row0 + j) * D;
+    uint16_t* dv_row = p.dv + static_cast<size_t>(k_row0 + j) * D + g * (D / 2);
+    uint16_t* dk_row = p.dk + static_cast<size_t>(k_row0 + j) * D + g * (D / 2);
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
-      const uint32_t colbase = which == 0 ? kColDV : kColDK;
+      const uint32_t colbase = (which == 0 ? kColDV : kColDK) + g * (D / 2);
       const float f = which == 0 ? 1.f : p.scale;
       uint16_t* dst_row = which == 0 ? dv_row : dk_row;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = 0; ch < D / 64; ++ch) {
         uint32_t v[32];
         if (live) {
           tmem_ld32(tmem + lane_base + colbase + ch * 32, v);
@@ -417,56 +467,85 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ dQ drain (thread = query)
-    // dQ_t (fp32, 128 queries x d) goes to the stage buffers of tile t in
-    // 32-column boxes of 128 rows x 128 bytes, 128-byte swizzled, then one
-    // thread adds the boxes into the global accumulator with TMA.
-    const int qq = tid - 128;
+    // ------------------------------------------------------------ dQ drain
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const bool leader = tid == 128;
-    for (int t = 0; t < ntiles; ++t) {
-      const int st = t & 1;
-      const int qb = list[t] >> 2;
-      if (!mbar_wait(bar.tile_done(), t & 1, p.status)) {
-        record_failure(p.status, kStatusTimeout, kSiteBwdDQ);
-        break;
-      }
-      tc_fence_after();
+    const int ln = tid - 256;  // TMEM lane this thread reads
+    int next_qb = ntiles > 0 ? (list[0] >> 2) : 0;  // read one tile ahead
+    if constexpr (kDqT) {
+      // lane = head dimension: each reduction of a warp covers 32 consecutive
+      // fp32 of one accumulator row (one 128-byte line)
+      for (int t = 0; t < ntiles; ++t) {
+        const int qb = next_qb;
+        if (t + 1 < ntiles) next_qb = list[t + 1] >> 2;
+        if (!mbar_wait(bar.tile_done(), t & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteBwdDQ);
+          break;
+        }
+        tc_fence_after();
+        float* dst = p.dq_accum + static_cast<size_t>(head_row0 + qb * kTile) * D + ln;
+        uint32_t v[64];
+        tmem_ld64(tmem + lane_base + kColDP, tmem + lane_base + kColDP + 32, v);
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kColDP + ch * 32, v);
-        const uint32_t box = (ch * 16384 < L::kTileBytes)
-                                 ? sQ + st * L::kTileBytes + ch * 16384
-                                 : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
+        for (int q = 0; q < 64; ++q) red_add_f32(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
+        tmem_ld64(tmem + lane_base + kColDP + 64, tmem + lane_base + kColDP + 96, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.dq_drained());
 #pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16)
-          st_shared_v4(box + sw128_offset(qq, c16), v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2],
-                       v[4 * c16 + 3]);
+        for (int q = 0; q < 64; ++q)
+          red_add_f32(dst + static_cast<size_t>(64 + q) * D, __uint_as_float(v[q]));
       }
-      tc_fence_before();
-      mbar_arrive(bar.dq_drained());
-      fence_proxy_async_smem();
-      drain_bar();
-      if (leader) {
+    } else {
+      // lane = query: dQ_t (fp32, 128 queries x d) goes to the stage buffers of
+      // tile t in 32-column boxes of 128 rows x 128 bytes, 128-byte swizzled,
+      // then one thread adds the boxes into the accumulator with TMA
+      const bool leader = tid == 256;
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t & 1;
+        const int qb = next_qb;
+        if (t + 1 < ntiles) next_qb = list[t + 1] >> 2;
+        if (!mbar_wait(bar.tile_done(), t & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteBwdDQ);
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kColDP + ch * 32, v);
           const uint32_t box = (ch * 16384 < L::kTileBytes)
                                    ? sQ + st * L::kTileBytes + ch * 16384
                                    : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
-          tma_reduce_add_2d(&mdq, box, ch * 32, head_row0 + qb * kTile);
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16)
+            st_shared_v4(box + sw128_offset(ln, c16), v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2],
+                         v[4 * c16 + 3]);
         }
-        bulk_commit_group();
-        bulk_wait_read_all();  // the stage buffers may be refilled now
-        if (t + 2 < ntiles) mbar_arrive(bar.q_empty(st));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.dq_drained());
+        fence_proxy_async_smem();
+        drain_bar();
+        if (leader) {
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            const uint32_t box = (ch * 16384 < L::kTileBytes)
+                                     ? sQ + st * L::kTileBytes + ch * 16384
+                                     : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
+            tma_reduce_add_2d(&mdq, box, ch * 32, head_row0 + qb * kTile);
+          }
+          bulk_commit_group();
+          bulk_wait_read_all();  // the stage buffers may be refilled now
+          if (t + 2 < ntiles) mbar_arrive(bar.q_empty(st));
+        }
       }
+      if (leader) bulk_wait_all();
     }
-    if (leader) bulk_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -496,7 +575,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
                                        L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.B * p.H * p.Tc);
-  bwd_kernel<D><<<grid, 320, L::kBytes, s>>>(mq, mk, mv, mdo, mdq, p);
+  bwd_kernel<D><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, mdo, mdq, p);
   return cudaGetLastError();
 }
 

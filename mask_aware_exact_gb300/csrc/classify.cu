@@ -23,7 +23,7 @@
 // by descending amount of work, which the attention kernels use as their
 // launch order (longest first).
 #include "internal.h"
-#include "../../include/flashmask.h"
+#include "flashmask.h"
 
 namespace fm {
 

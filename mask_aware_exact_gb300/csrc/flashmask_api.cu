@@ -6,7 +6,7 @@
 #include <mutex>
 
 #include "internal.h"
-#include "../../include/flashmask.h"
+#include "flashmask.h"
 
 namespace {
 

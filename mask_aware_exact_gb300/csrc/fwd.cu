@@ -4,16 +4,19 @@
 // abstract: warp specialisation overlapping TMA data movement with tensor-core
 // work, and block-wise matmul interleaved with softmax).
 //
-// One CTA = one (batch, head, query block). Warp roles:
-//   warps 0-3  softmax: thread t owns query row t (= TMEM lane t). Reads S from
-//              TMEM, applies the element mask on PARTIAL tiles, keeps the
-//              running max / sum in fp32 (log2 domain), writes P as bf16 into
-//              TMEM, rescales the O accumulator when the max grows by more than
-//              2^8 (lazy rescaling: exact after the final division), and
-//              finally writes O = acc / l and LSE.
-//   warp 4     TMA producer: Q once, then K and V tiles of each non-FULL key
-//              block into a two-stage ring.
-//   warp 5     MMA issuer (one thread): S_t = Q K_t^T (both operands in shared
+// One CTA = one (batch, head, query block). Warp roles (320 threads):
+//   warps 0-7  softmax, two warpgroups. Warpgroup g handles key columns
+//              [64g, 64g+64) of every tile; thread (g, r) owns query row r
+//              (= TMEM lane r). Each tile: read its half of S from TMEM, apply
+//              the element mask on PARTIAL tiles, exchange the half-row maxima
+//              through shared memory (one named barrier), keep the running max
+//              and partial sum in fp32 (log2 domain), write its half of P as
+//              bf16 into TMEM, and rescale its half of the O columns when the
+//              max grows by more than 2^8 (lazy rescaling: exact after the
+//              final division). Finally O = acc / l and LSE.
+//   warp 8     TMA producer: Q once, then K and V tiles of each non-FULL key
+//              block into a three-stage ring.
+//   warp 9     MMA issuer (one thread): S_t = Q K_t^T (both operands in shared
 //              memory, K-major) and O += P_{t-1} V_{t-1} (P from TMEM, V
 //              MN-major), so the next S overlaps the current softmax.
 //
@@ -22,13 +25,14 @@
 // another MMA may still read it: every reuse is ordered by an mbarrier.
 #include "internal.h"
 #include "ptx.cuh"
-#include "../../include/flashmask.h"
+#include "flashmask.h"
 
 namespace fm {
 
 namespace {
 
-constexpr int kStages = 2;
+constexpr int kStages = 3;
+constexpr int kThreads = 320;
 constexpr uint32_t kColS0 = 0, kColP0 = 256, kColO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -39,7 +43,8 @@ struct FwdLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
+  static constexpr int kRed = kV + kStages * kTileBytes;  // fp32 [2 parity][2 group][128]
+  static constexpr int kBar = kRed + 2 * 2 * kTile * 4;
   // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_ready
   static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
@@ -69,8 +74,11 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// The 256 softmax threads (both warpgroups).
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const FwdParams p) {
   using L = FwdLayout<D>;
@@ -94,10 +102,11 @@ __global__ void __launch_bounds__(192, 1)
   }
   const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK),
                  sV = smem_u32(smem + L::kV);
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
   const FwdBars bar{smem_u32(smem + L::kBar)};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -111,7 +120,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar.s_full(s), 1);
-      mbar_init(bar.p_full(s), 128);
+      mbar_init(bar.p_full(s), 8);
     }
     mbar_init(bar.o_ready(), 1);
     fence_barrier_init();
@@ -121,7 +130,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
       tma_prefetch_desc(&mq);
@@ -149,7 +158,7 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d(sV + st * L::kTileBytes + ch * 16384, &mv, ch * 64, krow, bar.v_full(st));
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
@@ -197,29 +206,52 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int row = tid;  // 0..127
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int g = warp >> 2;                 // warpgroup: key columns [64g, 64g+64)
+    const int row = (warp & 3) * 32 + lane;  // query row within the block = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    // The tile list and the bounds of a PARTIAL tile's key columns are read one
+    // tile ahead so their global-memory latency overlaps the current tile.
+    auto load_bounds = [&](int entry, int (&bd)[2][4]) {
+      if ((entry & 3) != FM_TILE_PARTIAL) return;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const size_t col = static_cast<size_t>(bm) * p.N + (entry >> 2) * kTile + 64 * g + 32 * k + lane;
+        bd[k][0] = p.mask.lts[col];
+        bd[k][1] = p.mask.lte[col];
+        bd[k][2] = p.mask.uts ? p.mask.uts[col] : 0;
+        bd[k][3] = p.mask.ute ? p.mask.ute[col] : 0;
+      }
+    };
+    int next_entry = ntiles > 0 ? list[0] : 0;
+    int next_bd[2][4];
+    load_bounds(next_entry, next_bd);
     for (int t = 0; t < ntiles; ++t) {
       const int sb = t & 1;
-      const int entry = list[t];
+      const int entry = next_entry;
+      int bd[2][4];
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bd[k][q] = next_bd[k][q];
+      if (t + 1 < ntiles) {
+        next_entry = list[t + 1];
+        load_bounds(next_entry, next_bd);
+      }
       const int kc = entry >> 2, lab = entry & 3;
-      // PARTIAL tile: lane l builds the masked-row bits of key column 32k + l
-      // for this warp's 32 rows; a bit transpose hands each lane its own row's
-      // bits over those 32 columns.
-      uint32_t mbits[4] = {0u, 0u, 0u, 0u};
+      // PARTIAL tile: lane l builds the masked-row bits of key column
+      // 64g + 32k + l for this warp's 32 rows; a bit transpose hands each
+      // lane its own row's bits over those 32 columns.
+      uint32_t mbits[2] = {0u, 0u};
       if (lab == FM_TILE_PARTIAL) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int j = kc * kTile + 32 * k + lane;
-          const size_t col = static_cast<size_t>(bm) * p.N + j;
-          const int lts = p.mask.lts[col], lte = p.mask.lte[col];
-          const int uts = p.mask.uts ? p.mask.uts[col] : 0, ute = p.mask.ute ? p.mask.ute[col] : 0;
-          mbits[k] = warp_transpose_bits(column_mask_bits(j, lts, lte, uts, ute,
-                                                          p.mask.causal != 0,
-                                                          r * kTile + 32 * warp));
+        for (int k = 0; k < 2; ++k) {
+          const int j = kc * kTile + 64 * g + 32 * k + lane;
+          mbits[k] = warp_transpose_bits(column_mask_bits(j, bd[k][0], bd[k][1], bd[k][2],
+                                                          bd[k][3], p.mask.causal != 0,
+                                                          r * kTile + 32 * (warp & 3)));
         }
       }
       if (!mbar_wait(bar.s_full(sb), (t >> 1) & 1, p.status)) {
@@ -228,28 +260,30 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kColS0 + sb * 128 + ch * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(v[i]);
+      uint32_t sv[64];
+      {
+        const uint32_t a = tmem + lane_base + kColS0 + sb * 128 + 64 * g;
+        tmem_ld64(a, a + 32, sv);
       }
       if (lab == FM_TILE_PARTIAL) {
 #pragma unroll
-        for (int jj = 0; jj < 128; ++jj)
-          s[jj] = ((mbits[jj >> 5] >> (jj & 31)) & 1u) ? -INFINITY : s[jj];
+        for (int jj = 0; jj < 64; ++jj)
+          sv[jj] = ((mbits[jj >> 5] >> (jj & 31)) & 1u) ? 0xff800000u : sv[jj];  // -inf
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mx0 = __uint_as_float(sv[0]), mx1 = __uint_as_float(sv[1]);
+      float mx2 = __uint_as_float(sv[2]), mx3 = __uint_as_float(sv[3]);
 #pragma unroll
-      for (int jj = 4; jj < 128; jj += 4) {
-        mx0 = fmaxf(mx0, s[jj]);
-        mx1 = fmaxf(mx1, s[jj + 1]);
-        mx2 = fmaxf(mx2, s[jj + 2]);
-        mx3 = fmaxf(mx3, s[jj + 3]);
+      for (int jj = 4; jj < 64; jj += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(sv[jj]));
+        mx1 = fmaxf(mx1, __uint_as_float(sv[jj + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sv[jj + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sv[jj + 3]));
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      // exchange half-row maxima (double-buffered by tile parity)
+      red[(sb * 2 + g) * kTile + row] = pm;
+      softmax_bar();
+      const float mx = fmaxf(pm, red[(sb * 2 + (g ^ 1)) * kTile + row]);
       const float m_new = fmaxf(m, mx);
       const bool rescale = m_new > m + kRescaleThreshold;
       float alpha = 1.f;
@@ -259,20 +293,17 @@ __global__ void __launch_bounds__(192, 1)
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
       float l0 = 0.f, l1 = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(s[ch * 32 + 2 * i], c, -m_use));
-          const float p1 = ex2(fmaf(s[ch * 32 + 2 * i + 1], c, -m_use));
-          l0 += p0;
-          l1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16p(tmem + lane_base + kColP0 + sb * 64 + ch * 16, pk);
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), c, -m_use));
+        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), c, -m_use));
+        l0 += p0;
+        l1 += p1;
+        pk[i] = pack_bf16x2(p0, p1);
       }
       l = l * alpha + (l0 + l1);
+      tmem_st32p(tmem + lane_base + kColP0 + sb * 64 + 32 * g, pk);
       if (t >= 1) {
         // O must hold every earlier P V before it is rescaled (and before the
         // P buffer of tile t+1 is rewritten)
@@ -284,9 +315,9 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
+          for (int ch = 0; ch < D / 64; ++ch) {
             uint32_t v[32];
-            const uint32_t addr = tmem + lane_base + kColO + ch * 32;
+            const uint32_t addr = tmem + lane_base + kColO + g * (D / 2) + ch * 32;
             tmem_ld32(addr, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
@@ -296,7 +327,8 @@ __global__ void __launch_bounds__(192, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar.p_full(sb));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.p_full(sb));
     }
     // ------------------------------------------------------------ epilogue
     if (ok && ntiles > 0) {
@@ -306,27 +338,36 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after();
     }
-    const bool has = ok && ntiles > 0 && l > 0.f;
-    const float inv = has ? 1.f / l : 0.f;
-    uint16_t* orow = p.o + static_cast<size_t>(q_row0 + row) * D;
+    // row sums through the exchange buffer of the parity the last tile did not
+    // use (its previous readers passed the last tile's barrier)
+    float* lsum = red + (ntiles & 1) * 2 * kTile;
+    lsum[g * kTile + row] = l;
+    softmax_bar();
+    const float ltot = l + lsum[(g ^ 1) * kTile + row];
+    const bool live = ok && ntiles > 0;
+    const bool has = live && ltot > 0.f;
+    const float inv = has ? 1.f / ltot : 0.f;
+    uint16_t* orow = p.o + static_cast<size_t>(q_row0 + row) * D + g * (D / 2);
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
+    for (int ch = 0; ch < D / 64; ++ch) {
       uint32_t v[32];
-      if (ok && ntiles > 0) {
-        tmem_ld32(tmem + lane_base + kColO + ch * 32, v);
+      if (live) {
+        tmem_ld32(tmem + lane_base + kColO + g * (D / 2) + ch * 32, v);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
       }
       store_row32_bf16(orow + ch * 32, v, inv);
     }
-    const float m_fin = (m == -INFINITY) ? 0.f : m;
-    p.lse[q_row0 + row] = has ? (m_fin + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    if (g == 0) {
+      const float m_fin = (m == -INFINITY) ? 0.f : m;
+      p.lse[q_row0 + row] = has ? (m_fin + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
+    }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -340,7 +381,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
                                        L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.B * p.H * p.Tr);
-  fwd_kernel<D><<<grid, 192, L::kBytes, s>>>(mq, mk, mv, p);
+  fwd_kernel<D><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
