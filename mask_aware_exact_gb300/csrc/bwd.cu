@@ -178,8 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const int BH = p.B * p.H;
-  const int rank = blockIdx.x / BH, bh = blockIdx.x % BH;
+  // Work item: head-major, longest key blocks of each head first, so the CTAs
+  // that run together reduce into one head's dQ accumulator, which then stays
+  // in L2 (fp32 reductions into L2-resident lines run at about twice the rate
+  // of reductions that reach DRAM).
+  const int bh = blockIdx.x / p.Tc, rank = blockIdx.x % p.Tc;
   const int b = bh / p.H, h = bh % p.H;
   const int bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
   const int kb = p.col_order[static_cast<size_t>(bm) * p.Tc + rank];
