@@ -149,6 +149,31 @@ fm_status flashmask_bwd_main(const void* q, const void* k, const void* v, const 
 fm_status flashmask_bwd_finalize(int B, int H, int Hm, int N, int d, float scale, void* dq,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/* Forward without any allocation or caller workspace: the paper has no
+ * counterpart; this exists for callers that cannot allocate device memory
+ * (inside a memory-pool or allocator callback, in runtimes that forbid
+ * cudaMalloc once started, or in plug-ins that are handed only their inputs and
+ * outputs). Same arguments and results as flashmask_fwd (with ws_classified =
+ * 0), but the classification tables live in a fixed scratch array of
+ * FM_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
+ * library holds until the process exits. Shapes whose tables would not fit
+ * (about B*Hm*(N/128)^2*10 bytes; N = 131072 with B*Hm = 1 fits) return
+ * FM_ERR_WORKSPACE before anything is launched. The call allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - The first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that first
+ *     call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents; each
+ *     call clears the status word it needs at zero and rewrites the tables.
+ *     Calls that may overlap on the GPU (other streams, other threads) race
+ *     on the array and must be serialised by the caller.
+ *   - A device-side wait failure is recorded in the scratch status word, which
+ *     callers cannot read; callers that need that report use flashmask_fwd. */
+#define FM_NOALLOC_SCRATCH_BYTES (16u << 20)
+fm_status flashmask_fwd_noalloc(const void* q, const void* k, const void* v, const fm_mask* mask,
+                                int B, int H, int N, int d, float scale, void* o, float* lse,
+                                void* stream);
+
 /* Synchronises `stream`, then reads and clears the workspace status word.
  * Returns FM_ERR_TIMEOUT if a kernel wait gave up since the last check,
  * FM_ERR_CUDA if the stream reports an error, FM_OK otherwise. If detail is

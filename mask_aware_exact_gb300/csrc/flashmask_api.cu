@@ -324,6 +324,65 @@ fm_status flashmask_bwd(const void* q, const void* k, const void* v, const void*
   return flashmask_bwd_finalize(B, H, mask->Hm, N, d, scale, dq, ws, ws_bytes, stream);
 }
 
+// ---------------------------------------------------------------- no-allocation forward
+// Some callers cannot allocate device memory at all: code running inside a
+// pre-reserved memory pool or an allocator callback, embedded runtimes that
+// forbid cudaMalloc after start-up, or plug-ins handed only their input and
+// output buffers. flashmask_fwd_noalloc serves them with a fixed scratch area
+// that lives in the library itself instead of a caller-provided workspace.
+}  // extern "C"
+
+namespace {
+
+// The scratch area (classification tables and the status word). Every GPU that
+// loads the library holds it until the process exits. In host code the name
+// only stands for the array; its device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FM_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+fm_status noalloc_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return FM_ERR_CUDA;
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return FM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fm_status flashmask_fwd_noalloc(const void* q, const void* k, const void* v, const fm_mask* mask,
+                                int B, int H, int N, int d, float scale, void* o, float* lse,
+                                void* stream) {
+  if (!q || !k || !v || !o || !lse || !mask_ok(mask)) return FM_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, mask->Hm, N, d)) return FM_ERR_UNSUPPORTED;
+  const fm_ws_layout L = make_layout(B, H, mask->Hm, N, d, 0);
+  if (L.total > FM_NOALLOC_SCRATCH_BYTES) return FM_ERR_WORKSPACE;  // beyond the fixed scratch
+  void* scratch = nullptr;
+  const fm_status st = noalloc_scratch_address(&scratch);
+  if (st != FM_OK) return st;
+  // the status word must start at zero; the tables are rewritten by the classification
+  if (cudaMemsetAsync(static_cast<char*>(scratch) + L.status, 0, 16,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FM_ERR_CUDA;
+  return flashmask_fwd(q, k, v, mask, B, H, N, d, scale, o, lse, scratch,
+                       FM_NOALLOC_SCRATCH_BYTES, 0, stream);
+}
+
 fm_status flashmask_check_status(void* ws, void* stream, int* detail) {
   if (detail) *detail = 0;
   if (!ws) return FM_ERR_WORKSPACE;

@@ -38,7 +38,8 @@ class FmWsLayout(ctypes.Structure):
 
 EXPORTED = ("flashmask_workspace_bytes", "flashmask_workspace_layout", "flashmask_classify",
             "flashmask_fwd", "flashmask_bwd", "flashmask_bwd_preprocess", "flashmask_bwd_main",
-            "flashmask_bwd_finalize", "flashmask_check_status", "flashmask_status_string")
+            "flashmask_bwd_finalize", "flashmask_fwd_noalloc", "flashmask_check_status",
+            "flashmask_status_string")
 
 _lib = None
 
@@ -71,6 +72,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.flashmask_bwd_main.restype = i
     L.flashmask_bwd_finalize.argtypes = [i, i, i, i, i, f, vp, vp, sz, vp]
     L.flashmask_bwd_finalize.restype = i
+    L.flashmask_fwd_noalloc.argtypes = [vp, vp, vp, ctypes.POINTER(_FmMask), i, i, i, i, f, vp, vp,
+                                        vp]
+    L.flashmask_fwd_noalloc.restype = i
     L.flashmask_check_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     L.flashmask_check_status.restype = i
     L.flashmask_status_string.argtypes = [i]
@@ -252,3 +256,21 @@ def read_classification(ws: torch.Tensor, B: int, Hm: int, N: int) -> dict:
         "col_list": region(L.col_list, B * Hm * Tc * Tr, np.int32, (B, Hm, Tc, Tr)),
         "col_order": region(L.col_order, B * Hm * Tc, np.int32, (B, Hm, Tc)),
     }
+
+
+def flashmask_fwd_noalloc(q, k, v, mask: DeviceMask, o, lse, scale=None, stream=None):
+    """Forward into caller-provided O and LSE with no workspace and no allocation.
+
+    The tables live in the library's fixed scratch array, so calls that may
+    overlap on the GPU must be serialised by the caller, and the first call on
+    a device must come before any stream capture. Shapes whose tables do not fit
+    raise FlashMaskError with FM_ERR_WORKSPACE."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _bf16(t, n)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    m = mask.c_struct()
+    _check(load().flashmask_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(m),
+                                        B, H, N, d, scale, o.data_ptr(), lse.data_ptr(),
+                                        _stream_ptr(stream)), "flashmask_fwd_noalloc")
+    return o, lse
