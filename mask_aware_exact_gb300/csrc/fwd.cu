@@ -4,31 +4,37 @@
 // abstract: warp specialisation overlapping TMA data movement with tensor-core
 // work, and block-wise matmul interleaved with softmax).
 //
-// The non-FULL key blocks of the query block are taken two at a time: one step
-// computes S = Q [K_a; K_b]^T as a single 128 x 256 product (a tcgen05 MMA with
-// N = 256 runs at the tensor core's full rate; N = 128 would run at half), then
-// O += P [V_a; V_b] as two K = 128 chains. A list of odd length ends with a
-// one-block step.
+// The non-FULL key blocks of the query block are visited one per step. The
+// tensor cores run ahead of the softmax: S_{j+2} = Q K_{j+2}^T is issued right
+// after O += P_j V_j, into one of three TMEM S regions, so that while the
+// softmax warps work on S_j the tensor pipe computes O += P_{j-1} V_{j-1} and
+// S_{j+1}. P_j is written as bf16 over S_j's own region.
 //
 // One CTA = one (batch, head, query block). Warp roles (320 threads):
-//   warps 0-7  softmax, two warpgroups. Warpgroup w owns S columns
-//              [128w, 128w+128) of every step (key block w of the pair); thread
-//              (w, r) owns query row r = TMEM lane r. Per step: read its S
-//              slice, apply the element mask on PARTIAL tiles, exchange the two
-//              partial row maxima through shared memory, keep the running max
-//              and partial sum in fp32 (log2 domain), compute its bf16 P slice
-//              in registers while the previous P V product still runs, then
-//              write it into TMEM and rescale its half of the O columns when the
-//              max grows by more than 2^8 (lazy rescaling: exact after the final
-//              division). Finally O = acc / l and LSE.
-//   warp 8     TMA producer: Q once; K pairs into a two-slot ring (one step
-//              ahead of the V loads); V blocks into a two-slot ring.
-//   warp 9     MMA issuer (one thread): S_{u+1} as soon as the softmax has read
-//              S_u, then O += P_u V_u.
+//   warps 0-7  softmax, two warpgroups. Thread (w, r) owns query row r (= TMEM
+//              lane r) and key columns [64w, 64w+64) of every block: it loads
+//              its 64 S values into registers, applies the element mask on
+//              PARTIAL tiles, exchanges its partial row maximum with the other
+//              warpgroup through shared memory, keeps the running max and
+//              partial sum in fp32 (log2 domain), and writes its bf16 P slice
+//              into TMEM. O is rescaled only when the max grows by more than 2^8
+//              (lazy rescaling: exact after the final division); warpgroup w
+//              rescales O columns [w d/2, (w+1) d/2). Finally O = acc / l and LSE.
+//   warp 8     TMA producer of Q (once) and K blocks (three-slot ring).
+//   warp 9     MMA issuer (one thread): S_0, S_1, then per step O += P_j V_j and
+//              S_{j+2} back to back after a single wait. An MMA issue returns
+//              only when the tensor pipe takes the instruction, and every
+//              mbarrier wait or commit in this thread leaves the pipe idle, so
+//              the thread waits once per step.
+//   warp 10    TMA producer of V blocks (three-slot ring).
+//   warp 11    gatekeeper (one thread): for step j waits until K_{j+2} and V_j
+//              have landed, O += P_{j-1} V_{j-1} has completed (S_{j+2} reuses
+//              that region) and P_j is written, then signals go(j).
 //
-// TMEM columns (512 allocated): S [0,256)  P [256,384)  O [384, 384+d).
-// Ordering: S_{u+1} is written after every softmax warp has loaded S_u
-// (s_free); P_{u+1} is written after O += P_u V_u has completed (o_ready).
+// TMEM columns (512 allocated): S regions [0,128) [128,256) [256,384), O [384, 384+d).
+// Ordering: S_{j+3} reuses the region of S_j / P_j once O += P_j V_j has
+// completed; the softmax of step j rescales O only after O += P_{j-1} V_{j-1}
+// has completed.
 #include "internal.h"
 #include "ptx.cuh"
 #include "flashmask.h"
@@ -37,23 +43,27 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 320;
-constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
+constexpr int kThreads = 384;
+constexpr int kSRegions = 3;  // TMEM S/P regions of 128 columns
+constexpr int kKSlots = 3, kVSlots = 3;
+constexpr uint32_t kColO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct FwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;  // one 128 x d bf16 tile
   static constexpr int kChunks = D / 64;            // 64-column (128-byte) TMA boxes
-  static constexpr int kChunkQ = 16384;             // 128 rows x 128 bytes
-  static constexpr int kChunkK = 32768;             // 256 rows x 128 bytes (a key pair)
+  static constexpr int kChunk = 16384;              // 128 rows x 128 bytes
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;          // 2 slots x (2 x kTileBytes)
-  static constexpr int kV = kK + 2 * 2 * kTileBytes;  // 2 slots x kTileBytes
-  static constexpr int kRed = kV + 2 * kTileBytes;    // fp32 [2 parity][2 groups][128]
+  static constexpr int kK = kQ + kTileBytes;             // kKSlots x kTileBytes
+  static constexpr int kV = kK + kKSlots * kTileBytes;   // kVSlots x kTileBytes
+  static constexpr int kRed = kV + kVSlots * kTileBytes;  // fp32 [2 parity][2 groups][128]
   static constexpr int kBar = kRed + 2 * 2 * kTile * 4;
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full, s_free, p_full, o_ready
-  static constexpr int kNumBars = 13;
+  // q_full, k_full[3], v_full[3], s_full[3], p_full[3], pv_done[3], go[3]. K slot,
+  // V slot and S region of block j are all j % 3, so "S_j done" also frees
+  // K slot j % 3 and "P_j V_j done" also frees V slot j % 3.
+  static_assert(kKSlots == kSRegions && kVSlots == kSRegions, "slots follow the S regions");
+  static constexpr int kNumBars = 1 + kKSlots + kVSlots + 4 * kSRegions;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
 };
@@ -62,13 +72,17 @@ struct FwdBars {
   uint32_t base;
   __device__ uint32_t q_full() const { return base; }
   __device__ uint32_t k_full(int s) const { return base + 8 * (1 + s); }
-  __device__ uint32_t k_empty(int s) const { return base + 8 * (3 + s); }
-  __device__ uint32_t v_full(int s) const { return base + 8 * (5 + s); }
-  __device__ uint32_t v_empty(int s) const { return base + 8 * (7 + s); }
-  __device__ uint32_t s_full() const { return base + 8 * 9; }
-  __device__ uint32_t s_free() const { return base + 8 * 10; }
-  __device__ uint32_t p_full() const { return base + 8 * 11; }
-  __device__ uint32_t o_ready() const { return base + 8 * 12; }
+  __device__ uint32_t v_full(int s) const { return base + 8 * (1 + kKSlots + s); }
+  __device__ uint32_t s_full(int r) const { return base + 8 * (1 + kKSlots + kVSlots + r); }
+  __device__ uint32_t p_full(int r) const {
+    return base + 8 * (1 + kKSlots + kVSlots + kSRegions + r);
+  }
+  __device__ uint32_t pv_done(int r) const {
+    return base + 8 * (1 + kKSlots + kVSlots + 2 * kSRegions + r);
+  }
+  __device__ uint32_t go(int r) const {
+    return base + 8 * (1 + kKSlots + kVSlots + 3 * kSRegions + r);
+  }
 };
 
 __device__ __forceinline__ void record_failure(int32_t* status, int bit, int site) {
@@ -146,7 +160,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
   const int r = p.row_order[static_cast<size_t>(bm) * p.Tr + rank];
   const int ntiles = p.row_count[static_cast<size_t>(bm) * p.Tr + r];
-  const int nsteps = (ntiles + 1) >> 1;
   const int32_t* list = p.row_list + (static_cast<size_t>(bm) * p.Tr + r) * p.Tc;
   const int head_row0 = bh * p.N;           // first row of this head in [B*H*N, d]
   const int q_row0 = head_row0 + r * kTile;  // first query row of the block
@@ -167,16 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     mbar_init(bar.q_full(), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar.k_full(s), 1);
-      mbar_init(bar.k_empty(s), 1);
-      mbar_init(bar.v_full(s), 1);
-      mbar_init(bar.v_empty(s), 1);
+    for (int s = 0; s < kKSlots; ++s) mbar_init(bar.k_full(s), 1);
+    for (int s = 0; s < kVSlots; ++s) mbar_init(bar.v_full(s), 1);
+    for (int g = 0; g < kSRegions; ++g) {
+      mbar_init(bar.s_full(g), 1);
+      mbar_init(bar.p_full(g), 8);
+      mbar_init(bar.pv_done(g), 1);
+      mbar_init(bar.go(g), 1);
     }
-    mbar_init(bar.s_full(), 1);
-    mbar_init(bar.s_free(), 8);
-    mbar_init(bar.p_full(), 8);
-    mbar_init(bar.o_ready(), 1);
     fence_barrier_init();
   }
   tc_fence_before();
@@ -185,250 +196,238 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer of Q, K
     if (lane == 0 && ntiles > 0) {
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mk);
-      tma_prefetch_desc(&mv);
       mbar_arrive_expect_tx(bar.q_full(), L::kTileBytes);
       for (int ch = 0; ch < L::kChunks; ++ch)
-        tma_load_2d(sQ + ch * L::kChunkQ, &mq, ch * 64, q_row0, bar.q_full());
-      // K pair of step u into slot u & 1 (rows 0-127: first block, 128-255: second)
-      auto load_k = [&](int u) -> bool {
-        const int slot = u & 1;
-        if (u >= 2 && !mbar_wait(bar.k_empty(slot), ((u >> 1) - 1) & 1, p.status)) {
+        tma_load_2d(sQ + ch * L::kChunk, &mq, ch * 64, q_row0, bar.q_full());
+      // K_j into slot j % 3 once S_{j-3} has completed
+      auto load_k = [&](int j) -> bool {
+        const int slot = j % kKSlots;
+        if (j >= kKSlots &&
+            !mbar_wait(bar.s_full(slot), ((j / kKSlots) - 1) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteFwdKEmpty);
           return false;
         }
-        const int nb = min(2, ntiles - 2 * u);
-        mbar_arrive_expect_tx(bar.k_full(slot), nb * L::kTileBytes);
-        for (int bb = 0; bb < nb; ++bb) {
-          const int krow = head_row0 + (list[2 * u + bb] >> 2) * kTile;
-          for (int ch = 0; ch < L::kChunks; ++ch)
-            tma_load_2d(sK + slot * 2 * L::kTileBytes + ch * L::kChunkK + bb * L::kChunkQ, &mk,
-                        ch * 64, krow, bar.k_full(slot));
-        }
+        mbar_arrive_expect_tx(bar.k_full(slot), L::kTileBytes);
+        const int krow = head_row0 + (list[j] >> 2) * kTile;
+        for (int ch = 0; ch < L::kChunks; ++ch)
+          tma_load_2d(sK + slot * L::kTileBytes + ch * L::kChunk, &mk, ch * 64, krow,
+                      bar.k_full(slot));
         return true;
       };
-      bool ok = load_k(0);
-      if (ok && nsteps > 1) ok = load_k(1);
-      for (int u = 0; ok && u < nsteps; ++u) {
-        const int nb = min(2, ntiles - 2 * u);
-        for (int bb = 0; bb < nb; ++bb) {
-          const int vi = 2 * u + bb, slot = vi & 1;
-          if (vi >= 2 && !mbar_wait(bar.v_empty(slot), ((vi >> 1) - 1) & 1, p.status)) {
-            record_failure(p.status, kStatusTimeout, kSiteFwdVEmpty);
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar.v_full(slot), L::kTileBytes);
-          const int vrow = head_row0 + (list[vi] >> 2) * kTile;
-          for (int ch = 0; ch < L::kChunks; ++ch)
-            tma_load_2d(sV + slot * L::kTileBytes + ch * L::kChunkQ, &mv, ch * 64, vrow,
-                        bar.v_full(slot));
+      bool ok = true;
+      for (int j = 0; ok && j < ntiles; ++j) ok = load_k(j);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ TMA producer of V
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&mv);
+      bool ok = true;
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int slot = j % kVSlots;
+        if (j >= kVSlots &&
+            !mbar_wait(bar.pv_done(slot), ((j / kVSlots) - 1) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdVEmpty);
+          ok = false;
+          break;
         }
-        if (ok && u + 2 < nsteps) ok = load_k(u + 2);
+        mbar_arrive_expect_tx(bar.v_full(slot), L::kTileBytes);
+        const int vrow = head_row0 + (list[j] >> 2) * kTile;
+        for (int ch = 0; ch < L::kChunks; ++ch)
+          tma_load_2d(sV + slot * L::kTileBytes + ch * L::kChunk, &mv, ch * 64, vrow,
+                      bar.v_full(slot));
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
-      auto issue_s = [&](int u) -> bool {
-        const int slot = u & 1;
-        if (!mbar_wait(bar.k_full(slot), (u >> 1) & 1, p.status)) {
-          record_failure(p.status, kStatusTimeout, kSiteFwdK);
-          return false;
+      // S_j; for j < 2 after waiting for K_j here, later ones after go(j - 2)
+      auto issue_s = [&](int j) -> bool {
+        const int slot = j % kKSlots, g = j % kSRegions;
+        if (j < 2) {
+          if (!mbar_wait(bar.k_full(slot), (j / kKSlots) & 1, p.status)) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdK);
+            return false;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
-        const int nb = min(2, ntiles - 2 * u);
-        const uint32_t idesc_s = nb == 2 ? idesc_bf16(128, 256, 0, 0) : idesc_bf16(128, 128, 0, 0);
-        const uint32_t kb = sK + slot * 2 * L::kTileBytes;
+        const uint32_t kb = sK + slot * L::kTileBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          mma_ss(tmem + kColS, sdesc_sw128(sQ + (k >> 2) * L::kChunkQ + (k & 3) * 32, 16, 1024),
-                 sdesc_sw128(kb + (k >> 2) * L::kChunkK + (k & 3) * 32, 16, 1024), idesc_s, k > 0);
+          const uint32_t off = (k >> 2) * L::kChunk + (k & 3) * 32;
+          mma_ss(tmem + 128 * g, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                 idesc_s, k > 0);
         }
-        if (u + 2 < nsteps) mma_commit(bar.k_empty(slot));
-        mma_commit(bar.s_full());
+        mma_commit(bar.s_full(g));  // also frees K slot j % 3
         return true;
       };
       bool ok = mbar_wait(bar.q_full(), 0, p.status);
       if (!ok) record_failure(p.status, kStatusTimeout, kSiteFwdQ);
       if (ok) ok = issue_s(0);
-      for (int u = 0; ok && u < nsteps; ++u) {
-        if (u + 1 < nsteps) {
-          // S_{u+1} overwrites S_u: wait until every softmax warp has loaded it
-          if (!mbar_wait(bar.s_free(), u & 1, p.status)) {
-            record_failure(p.status, kStatusTimeout, kSiteFwdS);
-            break;
-          }
-          if (!issue_s(u + 1)) break;
-        }
-        if (!mbar_wait(bar.p_full(), u & 1, p.status)) {
+      if (ok && ntiles > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int g = j % kSRegions, vs = j % kVSlots;
+        if (!mbar_wait(bar.go(g), (j / kSRegions) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteFwdP);
           break;
         }
-        const int nb = min(2, ntiles - 2 * u);
-        for (int bb = 0; bb < nb; ++bb) {
-          const int vi = 2 * u + bb, slot = vi & 1;
-          if (!mbar_wait(bar.v_full(slot), (vi >> 1) & 1, p.status)) {
-            record_failure(p.status, kStatusTimeout, kSiteFwdV);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t vb = sV + slot * L::kTileBytes;
+        tc_fence_after();
+        const uint32_t vb = sV + vs * L::kTileBytes;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColO, tmem + kColP + 64 * bb + 8 * k,
-                   sdesc_sw128(vb + k * 2048, 16384, 1024), idesc_pv, (vi > 0 || k > 0));
-          if (vi + 2 < ntiles) mma_commit(bar.v_empty(slot));
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + kColO, tmem + 128 * g + 8 * k, sdesc_sw128(vb + k * 2048, 16384, 1024),
+                 idesc_pv, (j > 0 || k > 0));
+        mma_commit(bar.pv_done(g));  // also frees V slot j % 3
+        if (j + 2 < ntiles) issue_s(j + 2);  // its region and K slot are cleared by go(j)
+      }
+    }
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ gatekeeper
+    if (lane == 0 && ntiles > 0) {
+      for (int j = 0; j < ntiles; ++j) {
+        const int g = j % kSRegions;
+        bool ok = true;
+        if (j + 2 < ntiles)
+          ok = mbar_wait(bar.k_full((j + 2) % kKSlots), ((j + 2) / kKSlots) & 1, p.status);
+        ok = ok && mbar_wait(bar.v_full(j % kVSlots), (j / kVSlots) & 1, p.status);
+        if (j >= 1)
+          ok = ok && mbar_wait(bar.pv_done((j - 1) % kSRegions), ((j - 1) / kSRegions) & 1,
+                               p.status);
+        ok = ok && mbar_wait(bar.p_full(g), (j / kSRegions) & 1, p.status);
+        if (!ok) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdP);
+          break;
         }
-        if (!ok) break;
-        mma_commit(bar.o_ready());
+        mbar_arrive(bar.go(g));
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int w = warp >> 2;                 // warpgroup: key block w of each pair
+    const int w = warp >> 2;                 // warpgroup: key columns [64w, 64w+64)
     const int row = (warp & 3) * 32 + lane;  // query row within the block = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    // This warpgroup's list entry of each step, read one step ahead.
-    auto entry_of = [&](int u) { return (2 * u + w < ntiles) ? list[2 * u + w] : -1; };
-    int next_entry = nsteps > 0 ? entry_of(0) : -1;
-    for (int u = 0; u < nsteps; ++u) {
+    int next_entry = ntiles > 0 ? list[0] : 0;  // read one step ahead
+    // After a failed wait the warp keeps stepping through the loop without
+    // touching TMEM, so that both warpgroups pass the same named barriers and
+    // the CTA can still reach its exit; `ok` is kept uniform across the warp.
+    for (int j = 0; j < ntiles; ++j) {
       const int entry = next_entry;
-      if (u + 1 < nsteps) next_entry = entry_of(u + 1);
-      const bool active = entry >= 0;  // a one-block last step leaves warpgroup 1 idle
-      // PARTIAL tile: lane l builds the masked-row bits of key column 32k + l
-      // for this warp's 32 rows; a bit transpose hands each lane its own row's
-      // bits over those 32 columns. The bound loads overlap the wait for S.
-      uint32_t mbits[4] = {0u, 0u, 0u, 0u};
-      if (active && (entry & 3) == FM_TILE_PARTIAL) {
+      if (j + 1 < ntiles) next_entry = list[j + 1];
+      const int g = j % kSRegions;
+      const bool partial = (entry & 3) == FM_TILE_PARTIAL;
+      // PARTIAL tile: lane l builds the masked-row bits of key column
+      // 64w + 32k + l for this warp's 32 rows; a bit transpose hands each lane
+      // its own row's bits over those 32 columns. The bound loads overlap the
+      // wait for S.
+      uint32_t mbits[2] = {0u, 0u};
+      if (partial) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int j = (entry >> 2) * kTile + 32 * k + lane;
-          const size_t col = static_cast<size_t>(bm) * p.N + j;
+        for (int k = 0; k < 2; ++k) {
+          const int jc = (entry >> 2) * kTile + 64 * w + 32 * k + lane;
+          const size_t col = static_cast<size_t>(bm) * p.N + jc;
           const int lts = p.mask.lts[col], lte = p.mask.lte[col];
           const int uts = p.mask.uts ? p.mask.uts[col] : 0, ute = p.mask.ute ? p.mask.ute[col] : 0;
-          mbits[k] = warp_transpose_bits(column_mask_bits(j, lts, lte, uts, ute,
+          mbits[k] = warp_transpose_bits(column_mask_bits(jc, lts, lte, uts, ute,
                                                           p.mask.causal != 0,
                                                           r * kTile + 32 * (warp & 3)));
         }
       }
-      if (!mbar_wait(bar.s_full(), u & 1, p.status)) {
-        record_failure(p.status, kStatusTimeout, kSiteFwdS);
-        ok = false;
-        break;
+      if (ok) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar.s_full(g), (j / kSRegions) & 1, p.status));
+        if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdS);
       }
-      tc_fence_after();
-      // pass 1: the row maximum of this warpgroup's 128 columns
+      uint32_t sv[64];
       float pm = -INFINITY;
-      const bool partial = (entry & 3) == FM_TILE_PARTIAL;
-      const uint32_t s_addr = tmem + lane_base + kColS + 128 * w;
-      if (active) {
+      if (ok) {
+        tc_fence_after();
+        const uint32_t s_addr = tmem + lane_base + 128 * g + 64 * w;
+        tmem_ld64(s_addr, s_addr + 32, sv);
+        if (partial) {
+#pragma unroll
+          for (int jj = 0; jj < 64; ++jj)
+            sv[jj] = ((mbits[jj >> 5] >> (jj & 31)) & 1u) ? 0xff800000u : sv[jj];
+        }
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sv[64];
-          tmem_ld64(s_addr + 64 * hh, s_addr + 64 * hh + 32, sv);
-          if (partial) {
-#pragma unroll
-            for (int jj = 0; jj < 64; ++jj)
-              sv[jj] = ((mbits[2 * hh + (jj >> 5)] >> (jj & 31)) & 1u) ? 0xff800000u : sv[jj];
-          }
-#pragma unroll
-          for (int jj = 0; jj < 64; jj += 4) {
-            mx0 = fmaxf(mx0, __uint_as_float(sv[jj]));
-            mx1 = fmaxf(mx1, __uint_as_float(sv[jj + 1]));
-            mx2 = fmaxf(mx2, __uint_as_float(sv[jj + 2]));
-            mx3 = fmaxf(mx3, __uint_as_float(sv[jj + 3]));
-          }
+        for (int jj = 0; jj < 64; jj += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sv[jj]));
+          mx1 = fmaxf(mx1, __uint_as_float(sv[jj + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sv[jj + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sv[jj + 3]));
         }
         pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
       }
-      // exchange the two partial row maxima (double-buffered by step parity)
-      red[((u & 1) * 2 + w) * kTile + row] = pm;
+      // exchange the two partial row maxima (double-buffered by step parity);
+      // the barrier also orders both warpgroups' S loads before any P store
+      // into the region
+      red[((j & 1) * 2 + w) * kTile + row] = pm;
       softmax_bar();
-      const float mx = fmaxf(pm, red[((u & 1) * 2 + (w ^ 1)) * kTile + row]);
-      const float m_new = fmaxf(m, mx);
-      const bool rescale = m_new > m + kRescaleThreshold;
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = ex2(m - m_new);
-        m = m_new;
-      }
-      const float m_use = (m == -INFINITY) ? 0.f : m;
-      // pass 2: P in registers (64 columns at a time) while O += P_{u-1} V_{u-1}
-      // may still run
-      float l0 = 0.f, l1 = 0.f;
-      uint32_t pk[64];
-      if (active) {
+      if (ok) {
+        const float mx = fmaxf(pm, red[((j & 1) * 2 + (w ^ 1)) * kTile + row]);
+        const float m_new = fmaxf(m, mx);
+        const bool rescale = m_new > m + kRescaleThreshold;
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = ex2(m - m_new);
+          m = m_new;
+        }
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        float l0 = 0.f, l1 = 0.f;
+        uint32_t pk[32];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sv[64];
-          tmem_ld64(s_addr + 64 * hh, s_addr + 64 * hh + 32, sv);
-          if (partial) {
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), c, -m_use));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), c, -m_use));
+          l0 += p0;
+          l1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        l = l * alpha + (l0 + l1);
+        // P_j over this warpgroup's part of S_j's region: keys [64w, 64w+64)
+        // as bf16 pairs in columns [32w, 32w+32) (the A operand of P V)
+        tmem_st32p(tmem + lane_base + 128 * g + 32 * w, pk);
+        if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+          // O is rescaled once O += P_{j-1} V_{j-1} has completed
+          ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done((j - 1) % kSRegions),
+                                                 ((j - 1) / kSRegions) & 1, p.status));
+          if (ok) {
+            tc_fence_after();
 #pragma unroll
-            for (int jj = 0; jj < 64; ++jj)
-              sv[jj] = ((mbits[2 * hh + (jj >> 5)] >> (jj & 31)) & 1u) ? 0xff800000u : sv[jj];
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), c, -m_use));
-            const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), c, -m_use));
-            l0 += p0;
-            l1 += p1;
-            pk[32 * hh + i] = pack_bf16x2(p0, p1);
+            for (int ch = 0; ch < kOCols / 32; ++ch)
+              tmem_scale_cols<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, alpha);
+          } else if (lane == 0) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdO);
           }
         }
+        tmem_st_wait();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar.s_free());  // S may be overwritten by the next step
-      l = l * alpha + (l0 + l1);
-      if (u >= 1) {
-        // the P region and O are free once O += P_{u-1} V_{u-1} has completed
-        if (!mbar_wait(bar.o_ready(), (u - 1) & 1, p.status)) {
-          record_failure(p.status, kStatusTimeout, kSiteFwdO);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      if (active) {
-        tmem_st32p(tmem + lane_base + kColP + 64 * w, &pk[0]);
-        tmem_st32p(tmem + lane_base + kColP + 64 * w + 32, &pk[32]);
-      }
-      if (u >= 1 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int ch = 0; ch < kOCols / 32; ++ch)
-          tmem_scale_cols<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, alpha);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.p_full());
+      if (lane == 0) mbar_arrive(bar.p_full(g));
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && nsteps > 0) {
-      if (!mbar_wait(bar.o_ready(), (nsteps - 1) & 1, p.status)) {
-        record_failure(p.status, kStatusTimeout, kSiteFwdO);
-        ok = false;
-      }
+    if (ok && ntiles > 0) {
+      const int jl = ntiles - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(jl % kSRegions), (jl / kSRegions) & 1,
+                                             p.status));
+      if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdO);
       tc_fence_after();
     }
     // row sums through the exchange buffer of the parity the last step did not
     // use (its previous readers passed the last step's barrier)
-    float* lsum = red + (nsteps & 1) * 2 * kTile;
+    float* lsum = red + (ntiles & 1) * 2 * kTile;
     lsum[w * kTile + row] = l;
     softmax_bar();
     const float ltot = l + lsum[(w ^ 1) * kTile + row];
-    const bool live = ok && nsteps > 0;
+    const bool live = ok && ntiles > 0;
     const bool has = live && ltot > 0.f;
     const float inv = has ? 1.f / ltot : 0.f;
     uint16_t* orow = p.o + static_cast<size_t>(q_row0 + row) * D + w * kOCols;

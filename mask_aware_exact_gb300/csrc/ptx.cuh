@@ -53,11 +53,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test: true iff the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the phase with the given parity to complete. Returns false if the
 // wall-time limit ran out first, or as soon as `abort_word` (the device status
 // word; may be null) is nonzero because some other wait of the grid gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const int32_t* abort_word) {
+  if (mbar_test_wait(bar, parity)) return true;  // already complete: no suspend
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
