@@ -13,11 +13,13 @@
 //                 dV  += P^T dO             (A from TMEM)
 //                 dS^T = P^T (dP^T - D)     -> bf16 in shared memory
 //                 dK  += dS^T Q             (dS^T K-major)
-//                 dQ_t                      -> TMEM -> fp32 global accumulator
-//               d = 128: dQ_t^T = K^T dS^T (M = d), one head dimension per TMEM
-//               lane, reduced from registers with coalesced fp32 adds.
-//               d = 64: dQ_t = dS K (M = queries), through the tile's own Q/dO
-//               stage buffers and a TMA bulk reduce-add.
+//                 dQ_t = dS K               -> TMEM -> the tile's own Q/dO stage
+//                                              buffers -> TMA bulk reduce-add into
+//                                              the fp32 global accumulator
+//               (Reductions issued as red.global from the drain warps were
+//               measured to slow the compute warps' exponentials and TMEM loads
+//               about 2.4x on GB300; the bulk reduce leaves that traffic to the
+//               TMA engine.)
 //   dq_convert  dQ = bf16(scale * accumulator).
 //
 // Warp roles of bwd_kernel (448 threads): warps 0-7 compute, two warpgroups;
@@ -105,9 +107,6 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -171,10 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                const __grid_constant__ CUtensorMap mdq, const BwdParams p) {
   using L = BwdLayout<D>;
-  // d = 128: dQ^T lives in TMEM with one head dimension per lane and is reduced
-  // into the accumulator straight from registers (coalesced rows). d = 64: dQ
-  // (one query per lane) goes out through the stage buffers and a TMA reduce.
-  constexpr bool kDqT = (D == 128);
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -261,8 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t id_st = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t id_kd = idesc_bf16(128, D, 0, 1);    // dV, dK
-      constexpr uint32_t id_dq = kDqT ? idesc_bf16(128, 128, 1, 1)   // dQ^T (M = d = 128)
-                                      : idesc_bf16(128, D, 1, 1);    // dQ (M = queries)
+      constexpr uint32_t id_dq = idesc_bf16(128, D, 1, 1);    // dQ (M = queries)
       bool ok = mbar_wait(bar.kv_full(), 0, p.status);
       if (!ok) record_failure(p.status, kStatusTimeout, kSiteBwdKV);
       for (int t = 0; ok && t < ntiles; ++t) {
@@ -317,24 +311,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + kColDK, sdesc_sw128(sDS + off, 16, 1024),
                  sdesc_sw128(q + k * 2048, 16384, 1024), id_kd, (t > 0 || k > 0));
         }
-        if constexpr (kDqT) {
-          // dQ_t^T = K^T dS^T: A = the K tile read MN-major (M = d), B = dS^T read
-          // MN-major (N = queries); rows of the result are head dimensions
+        // dQ_t = dS K: A = dS^T read MN-major (M = queries), B = K read MN-major
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + kColDP, sdesc_sw128(sK + k * 2048, 16384, 1024),
-                   sdesc_sw128(sDS + k * 2048, 16384, 1024), id_dq, k > 0);
-        } else {
-          // dQ_t = dS K: A = dS^T read MN-major (M = queries), B = K read MN-major
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + kColDP, sdesc_sw128(sDS + k * 2048, 16384, 1024),
-                   sdesc_sw128(sK + k * 2048, 16384, 1024), id_dq, k > 0);
-        }
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + kColDP, sdesc_sw128(sDS + k * 2048, 16384, 1024),
+                 sdesc_sw128(sK + k * 2048, 16384, 1024), id_dq, k > 0);
         mma_commit(bar.tile_done());
-        // Q_t and dO_t are no longer read; with dQ^T drained from registers the
-        // stage goes back to the producer at once
-        if (kDqT && t + 2 < ntiles) mma_commit(bar.q_empty(st));
       }
     }
   } else if (warp < 8) {
@@ -474,76 +456,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int ln = tid - 256;  // TMEM lane this thread reads
     int next_qb = ntiles > 0 ? (list[0] >> 2) : 0;  // read one tile ahead
-    if constexpr (kDqT) {
-      // lane = head dimension: each reduction of a warp covers 32 consecutive
-      // fp32 of one accumulator row (one 128-byte line)
-      for (int t = 0; t < ntiles; ++t) {
-        const int qb = next_qb;
-        if (t + 1 < ntiles) next_qb = list[t + 1] >> 2;
-        if (!mbar_wait(bar.tile_done(), t & 1, p.status)) {
-          record_failure(p.status, kStatusTimeout, kSiteBwdDQ);
-          break;
-        }
-        tc_fence_after();
-        float* dst = p.dq_accum + static_cast<size_t>(head_row0 + qb * kTile) * D + ln;
-        uint32_t v[64];
-        tmem_ld64(tmem + lane_base + kColDP, tmem + lane_base + kColDP + 32, v);
-#pragma unroll
-        for (int q = 0; q < 64; ++q) red_add_f32(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]));
-        tmem_ld64(tmem + lane_base + kColDP + 64, tmem + lane_base + kColDP + 96, v);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar.dq_drained());
-#pragma unroll
-        for (int q = 0; q < 64; ++q)
-          red_add_f32(dst + static_cast<size_t>(64 + q) * D, __uint_as_float(v[q]));
+    // lane = query: dQ_t (fp32, 128 queries x d) goes to the stage buffers of
+    // tile t in 32-column boxes of 128 rows x 128 bytes, 128-byte swizzled,
+    // then one thread adds the boxes into the accumulator with TMA
+    const bool leader = tid == 256;
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t & 1;
+      const int qb = next_qb;
+      if (t + 1 < ntiles) next_qb = list[t + 1] >> 2;
+      if (!mbar_wait(bar.tile_done(), t & 1, p.status)) {
+        record_failure(p.status, kStatusTimeout, kSiteBwdDQ);
+        break;
       }
-    } else {
-      // lane = query: dQ_t (fp32, 128 queries x d) goes to the stage buffers of
-      // tile t in 32-column boxes of 128 rows x 128 bytes, 128-byte swizzled,
-      // then one thread adds the boxes into the accumulator with TMA
-      const bool leader = tid == 256;
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t & 1;
-        const int qb = next_qb;
-        if (t + 1 < ntiles) next_qb = list[t + 1] >> 2;
-        if (!mbar_wait(bar.tile_done(), t & 1, p.status)) {
-          record_failure(p.status, kStatusTimeout, kSiteBwdDQ);
-          break;
-        }
-        tc_fence_after();
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kColDP + ch * 32, v);
+        const uint32_t box = (ch * 16384 < L::kTileBytes)
+                                 ? sQ + st * L::kTileBytes + ch * 16384
+                                 : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16)
+          st_shared_v4(box + sw128_offset(ln, c16), v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2],
+                       v[4 * c16 + 3]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.dq_drained());
+      fence_proxy_async_smem();
+      drain_bar();
+      if (leader) {
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + kColDP + ch * 32, v);
           const uint32_t box = (ch * 16384 < L::kTileBytes)
                                    ? sQ + st * L::kTileBytes + ch * 16384
                                    : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
-#pragma unroll
-          for (int c16 = 0; c16 < 8; ++c16)
-            st_shared_v4(box + sw128_offset(ln, c16), v[4 * c16], v[4 * c16 + 1], v[4 * c16 + 2],
-                         v[4 * c16 + 3]);
+          tma_reduce_add_2d(&mdq, box, ch * 32, head_row0 + qb * kTile);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar.dq_drained());
-        fence_proxy_async_smem();
-        drain_bar();
-        if (leader) {
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            const uint32_t box = (ch * 16384 < L::kTileBytes)
-                                     ? sQ + st * L::kTileBytes + ch * 16384
-                                     : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
-            tma_reduce_add_2d(&mdq, box, ch * 32, head_row0 + qb * kTile);
-          }
-          bulk_commit_group();
-          bulk_wait_read_all();  // the stage buffers may be refilled now
-          if (t + 2 < ntiles) mbar_arrive(bar.q_empty(st));
-        }
+        bulk_commit_group();
+        bulk_wait_read_all();  // the stage buffers may be refilled now
+        if (t + 2 < ntiles) mbar_arrive(bar.q_empty(st));
       }
-      if (leader) bulk_wait_all();
     }
+    if (leader) bulk_wait_all();
   }
 
   tc_fence_before();
