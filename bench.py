@@ -38,9 +38,17 @@ METRIC = "effective TFLOP/s (unmasked FLOPs) fwd+bwd at 1 GB300; % of dense BF16
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
-# DRAM bytes per launch of the backward main kernel from an ncu capture (see
-# profiles/), valid only for the kernel source it was measured on.
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the attention kernels on the 32K
+# document workload, keyed by kernel and a hash of the kernel source they were
+# measured on (a changed kernel reports null). Captured with ncu on the same
+# workload at H = 8 (profiles/bwd_kernel_document_b1h8n32768d128.md,
+# profiles/fwd_kernel_document_b1h8n32768d128.md) and scaled by 4 to H = 32:
+# every head is an independent unit of identical work, so traffic grows in
+# proportion to the heads.
+NCU_TRAFFIC = {
+    "bwd_main@e03f310508ff": 4 * (405.983488e6 + 220.970240e6),
+    "fwd@16dc441880ce": 4 * (201.948672e6 + 49.610752e6),
+}
 
 
 def peaks():
