@@ -38,16 +38,19 @@ METRIC = "effective TFLOP/s (unmasked FLOPs) fwd+bwd at 1 GB300; % of dense BF16
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
-# DRAM bytes (read + write) per launch of the attention kernels on the 32K
-# document workload, keyed by kernel and a hash of the kernel source they were
-# measured on (a changed kernel reports null). Captured with ncu on the same
+# DRAM bytes (read + write) per launch of the attention kernels, keyed by
+# kernel, a hash of the kernel source they were measured on (a changed kernel
+# reports null) and workload. Captured with ncu on the same
 # workload at H = 8 (profiles/bwd_kernel_document_b1h8n32768d128.md,
 # profiles/fwd_kernel_document_b1h8n32768d128.md) and scaled by 4 to H = 32:
 # every head is an independent unit of identical work, so traffic grows in
 # proportion to the heads.
+# Heads per chunk of the host-buffer pipeline the end-to-end leg times.
+E2E_CHUNK_HEADS = 4
+
 NCU_TRAFFIC = {
-    "bwd_main@e03f310508ff": 4 * (405.983488e6 + 220.970240e6),
-    "fwd@16dc441880ce": 4 * (201.948672e6 + 49.610752e6),
+    "bwd_main@e03f310508ff@document_b1h32n32768d128": 4 * (405.983488e6 + 220.970240e6),
+    "fwd@16dc441880ce@document_b1h32n32768d128": 4 * (201.948672e6 + 49.610752e6),
 }
 
 
@@ -230,25 +233,25 @@ def run_native(args):
     value = agg["throughput"] / 1e12
     ms_per_step = agg["max_elapsed_s"] / K * 1e3
 
-    # ---------------- end to end: pinned host buffers in, results back to host
-    out_h = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-             for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-    mask_h = {n: getattr(mask, n).cpu().pin_memory() for n in ("lts", "lte", "uts", "ute")
-              if getattr(mask, n) is not None}
+    # ---------------- end to end: pinned host buffers in, results back to host,
+    # through the library's host-buffer entry point (copies overlapped with the
+    # kernels in head chunks)
+    chunk = E2E_CHUNK_HEADS if H % E2E_CHUNK_HEADS == 0 else H
+    mask_h = fm.HostMask.from_spec(w.mask, pin=True)
+    hws = fm.alloc_host_workspace(B, H, mask_h.Hm, N, d, chunk, device=dev)
+    out_h = (torch.empty(q_h.shape, dtype=torch.bfloat16, pin_memory=True),
+             torch.empty((B, H, N), dtype=torch.float32, pin_memory=True),
+             torch.empty(q_h.shape, dtype=torch.bfloat16, pin_memory=True),
+             torch.empty(q_h.shape, dtype=torch.bfloat16, pin_memory=True),
+             torch.empty(q_h.shape, dtype=torch.bfloat16, pin_memory=True))
+    mvecs = [t for t in (mask_h.lts, mask_h.lte, mask_h.uts, mask_h.ute) if t is not None]
     h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, do_h)) + \
-        sum(t.numel() * t.element_size() for t in mask_h.values())
-    d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+        sum(t.numel() * t.element_size() for t in mvecs)
+    d2h = sum(t.numel() * t.element_size() for t in out_h)
 
     def e2e_step():
-        for dst, src in ((q, q_h), (k, k_h), (v, v_h), (do, do_h)):
-            dst.copy_(src, non_blocking=True)
-        for n, t in mask_h.items():
-            getattr(mask, n).copy_(t, non_blocking=True)
-        fm.flashmask_fwd(q, k, v, mask, ws, scale=scale, o=o, lse=lse, ws_classified=False)
-        fm.flashmask_bwd(q, k, v, o, lse, do, mask, ws, scale=scale, dq=dq, dk=dk, dv=dv,
-                         ws_classified=True)
-        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            out_h[n].copy_(t, non_blocking=True)
+        fm.flashmask_fwd_bwd_host(q_h, k_h, v_h, do_h, mask_h, hws, chunk, scale=scale, out=out_h,
+                                  stream=stream)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -264,9 +267,7 @@ def run_native(args):
     R.barrier()
     e2e_s = a0.elapsed_time(a1) / 1e3
     e2e_agg = R.aggregate_throughput(fl["total"] * K2, e2e_s, dev)
-    st, site = fm.flashmask_check_status(ws)
-    if st != fm.FM_OK:
-        raise RuntimeError(f"device status {st} at site {site} in the end-to-end region")
+    del hws
 
     pk, pk_src = peaks()
     peak_dense = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
@@ -276,7 +277,7 @@ def run_native(args):
     dom_flops = fl["bwd"] if dom == "bwd_main" else fl["fwd"]
     achieved = dom_flops / (per[dom] / 1e3) / 1e12
     src_hash = kernel_source_hash(("bwd.cu", "ptx.cuh") if dom == "bwd_main" else ("fwd.cu", "ptx.cuh"))
-    traffic = NCU_TRAFFIC.get(f"{dom}@{src_hash}")
+    traffic = NCU_TRAFFIC.get(f"{dom}@{src_hash}@{w.name}")
 
     result = None
     if rank == 0:
@@ -314,6 +315,7 @@ def run_native(args):
                          "traffic": traffic},
             "e2e": {"value": round(e2e_agg["throughput"] / 1e12, 2), "unit": UNIT,
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "api": "flashmask_fwd_bwd_host", "chunk_heads": chunk,
                     "ms_per_step": round(e2e_agg["max_elapsed_s"] / K2 * 1e3, 4)},
             "gpu_launches": 7 * K,
             "clocks": clk,

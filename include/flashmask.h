@@ -174,6 +174,32 @@ fm_status flashmask_fwd_noalloc(const void* q, const void* k, const void* v, con
                                 int B, int H, int N, int d, float scale, void* o, float* lse,
                                 void* stream);
 
+/* Forward and backward between HOST buffers, for callers whose tensors live in
+ * host memory (the pages have no counterpart; the computation is exactly
+ * flashmask_classify + flashmask_fwd + flashmask_bwd). The heads are cut into
+ * chunks of `chunk_heads` consecutive heads of one batch entry (heads are
+ * independent) and three streams overlap the copy of chunk c+1 to the device,
+ * the kernels of chunk c and the copy of chunk c-1 back to the host, in three
+ * slots carved from the device workspace `dev_ws` (>= the size
+ * flashmask_host_workspace_bytes() returns for the same shape and chunk, 256-byte
+ * aligned; the function returns 0 for an unsupported shape or chunk).
+ *   Host pointers: q, k, v, dout [B,H,N,d] bf16; mask->lts/lte/uts/ute
+ *   [B,Hm,N] int32; outputs o, dq, dk, dv [B,H,N,d] bf16 and lse [B,H,N] fp32.
+ *   Page-locked host memory (cudaHostAlloc, torch pin_memory) lets the copies
+ *   run concurrently with the kernels; pageable memory works but serialises.
+ *   chunk_heads must divide H and either divide H / Hm or be a multiple of it
+ *   (a chunk reads whole mask heads); otherwise FM_ERR_UNSUPPORTED.
+ *   The call orders its work after what is already queued on `stream` and
+ *   returns only when every output is in host memory (or with the first error;
+ *   a kernel wait that gave up gives FM_ERR_TIMEOUT). It allocates no device
+ *   memory; three streams and a few events are created once per device and
+ *   kept, and calls on one device are serialised by a lock. */
+size_t flashmask_host_workspace_bytes(int B, int H, int Hm, int N, int d, int chunk_heads);
+fm_status flashmask_fwd_bwd_host(const void* q, const void* k, const void* v, const void* dout,
+                                 const fm_mask* mask, int B, int H, int N, int d, float scale,
+                                 void* o, float* lse, void* dq, void* dk, void* dv, void* dev_ws,
+                                 size_t ws_bytes, int chunk_heads, void* stream);
+
 /* Synchronises `stream`, then reads and clears the workspace status word.
  * Returns FM_ERR_TIMEOUT if a kernel wait gave up since the last check,
  * FM_ERR_CUDA if the stream reports an error, FM_OK otherwise. If detail is

@@ -38,8 +38,8 @@ class FmWsLayout(ctypes.Structure):
 
 EXPORTED = ("flashmask_workspace_bytes", "flashmask_workspace_layout", "flashmask_classify",
             "flashmask_fwd", "flashmask_bwd", "flashmask_bwd_preprocess", "flashmask_bwd_main",
-            "flashmask_bwd_finalize", "flashmask_fwd_noalloc", "flashmask_check_status",
-            "flashmask_status_string")
+            "flashmask_bwd_finalize", "flashmask_fwd_noalloc", "flashmask_host_workspace_bytes",
+            "flashmask_fwd_bwd_host", "flashmask_check_status", "flashmask_status_string")
 
 _lib = None
 
@@ -75,6 +75,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.flashmask_fwd_noalloc.argtypes = [vp, vp, vp, ctypes.POINTER(_FmMask), i, i, i, i, f, vp, vp,
                                         vp]
     L.flashmask_fwd_noalloc.restype = i
+    L.flashmask_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    L.flashmask_host_workspace_bytes.restype = sz
+    L.flashmask_fwd_bwd_host.argtypes = [vp, vp, vp, vp, ctypes.POINTER(_FmMask), i, i, i, i, f, vp,
+                                         vp, vp, vp, vp, vp, sz, i, vp]
+    L.flashmask_fwd_bwd_host.restype = i
     L.flashmask_check_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     L.flashmask_check_status.restype = i
     L.flashmask_status_string.argtypes = [i]
@@ -274,3 +279,76 @@ def flashmask_fwd_noalloc(q, k, v, mask: DeviceMask, o, lse, scale=None, stream=
                                         B, H, N, d, scale, o.data_ptr(), lse.data_ptr(),
                                         _stream_ptr(stream)), "flashmask_fwd_noalloc")
     return o, lse
+
+
+# ---------------------------------------------------------------- host buffers
+@dataclass
+class HostMask:
+    """Boundary vectors in host memory (contiguous int32 [B, Hm, N] CPU tensors,
+    page-locked when made by from_spec) plus the causal flag."""
+
+    lts: torch.Tensor
+    lte: torch.Tensor
+    uts: torch.Tensor | None
+    ute: torch.Tensor | None
+    causal: bool
+
+    @property
+    def Hm(self) -> int:
+        return self.lts.shape[1]
+
+    @staticmethod
+    def from_spec(spec, pin=True) -> "HostMask":
+        def t(a):
+            if a is None:
+                return None
+            x = torch.from_numpy(np.ascontiguousarray(a, np.int32))
+            return x.pin_memory() if pin else x
+        return HostMask(t(spec.lts), t(spec.lte), t(spec.uts), t(spec.ute), bool(spec.causal))
+
+    def c_struct(self) -> _FmMask:
+        for v in (self.lts, self.lte, self.uts, self.ute):
+            if v is not None:
+                if v.dtype != torch.int32 or v.is_cuda or not v.is_contiguous():
+                    raise ValueError("host mask vectors must be contiguous int32 CPU tensors")
+        p = lambda v: None if v is None else v.data_ptr()
+        return _FmMask(p(self.lts), p(self.lte), p(self.uts), p(self.ute), self.Hm, int(self.causal))
+
+
+def flashmask_host_workspace_bytes(B, H, Hm, N, d, chunk_heads) -> int:
+    return int(load().flashmask_host_workspace_bytes(B, H, Hm, N, d, chunk_heads))
+
+
+def alloc_host_workspace(B, H, Hm, N, d, chunk_heads, device="cuda") -> torch.Tensor:
+    n = flashmask_host_workspace_bytes(B, H, Hm, N, d, chunk_heads)
+    if n == 0:
+        raise FlashMaskError(FM_ERR_UNSUPPORTED, "flashmask_host_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def flashmask_fwd_bwd_host(q, k, v, do, mask: HostMask, dev_ws, chunk_heads, scale=None,
+                           out=None, stream=None):
+    """Forward and backward between host tensors (bf16 [B,H,N,d], page-locked for
+    the copies to overlap). Returns (O, LSE, dQ, dK, dV) on the host; `out` may
+    hold preallocated host tensors in that order. Blocks until the results are
+    in host memory."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do")):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous bf16 CPU tensor")
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        pin = q.is_pinned()
+        mk = lambda shape, dt: torch.empty(shape, dtype=dt, pin_memory=pin)
+        out = (mk(q.shape, torch.bfloat16), mk((B, H, N), torch.float32), mk(q.shape, torch.bfloat16),
+               mk(q.shape, torch.bfloat16), mk(q.shape, torch.bfloat16))
+    o, lse, dq, dk, dv = out
+    m = mask.c_struct()
+    _check(load().flashmask_fwd_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                         ctypes.byref(m), B, H, N, d, scale, o.data_ptr(),
+                                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                         dev_ws.data_ptr(), dev_ws.numel(), int(chunk_heads),
+                                         _stream_ptr(stream)), "flashmask_fwd_bwd_host")
+    return o, lse, dq, dk, dv
