@@ -24,8 +24,10 @@
  *   Q, K, V, O, dO, dQ, dK, dV : bf16  [B, H, N, d]
  *   LSE                        : fp32  [B, H, N]     (natural log)
  *   LTS, LTE, UTS, UTE         : int32 [B, Hm, N]    (head h reads mask head h / (H / Hm))
- * Supported shapes: d in {64, 128}; N a positive multiple of 128; H % Hm == 0;
- * B * H * N < 2^31. Other shapes return FM_ERR_UNSUPPORTED.
+ * Supported shapes: d in {64, 128}; any N >= 1 (the last 128-row block of a
+ * sequence whose length is not a multiple of 128 is short; its missing rows and
+ * keys take no part); H % Hm == 0; B * H * Npad < 2^31 with Npad = N rounded up
+ * to a multiple of 128. Other shapes return FM_ERR_UNSUPPORTED.
  *
  * Workspace: the library never allocates. The caller passes one device buffer
  * of at least flashmask_workspace_bytes(...) bytes, aligned to 256 bytes. It
@@ -54,7 +56,7 @@ extern "C" {
 typedef enum {
   FM_OK = 0,
   FM_ERR_INVALID_ARG = 1,  /* null pointer, negative size, scale not finite, ...   */
-  FM_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, N % 128 != 0, H % Hm != 0, ...    */
+  FM_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, N < 1, H % Hm != 0, ...           */
   FM_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed          */
   FM_ERR_TIMEOUT = 4,      /* a kernel wait gave up (see flashmask_check_status)   */
   FM_ERR_WORKSPACE = 5     /* workspace null, misaligned or smaller than required  */
@@ -93,10 +95,11 @@ typedef struct {
  *   col_count int32  [B,Hm,Tc]           non-FULL tiles per key block
  *   col_list  int32  [B,Hm,Tc,Tr]        (query block << 2) | label, ascending
  *   col_order int32  [B,Hm,Tc]           key blocks by descending col_count
- *   lse2      fp32   [B,H,N]      [bwd]  LSE * log2(e) (+inf for a fully masked row)
- *   delta     fp32   [B,H,N]      [bwd]  rowsum(dO * O)
- *   dq_accum  fp32   [B,H,N,d]    [bwd]  dQ accumulator
- * with Tr = Tc = N / 128. */
+ *   lse2      fp32   [B,H,Npad]   [bwd]  LSE * log2(e) (+inf for a fully masked
+ *                                       row and for the padding rows n >= N)
+ *   delta     fp32   [B,H,Npad]   [bwd]  rowsum(dO * O) (0 on padding rows)
+ *   dq_accum  fp32   [B,H,Npad,d] [bwd]  dQ accumulator
+ * with Tr = Tc = ceil(N / 128) and Npad = 128 * Tr. */
 typedef struct {
   size_t status, minmax, labels, labels_t, row_count, row_list, row_order, col_count, col_list,
       col_order, lse2, delta, dq_accum, total;

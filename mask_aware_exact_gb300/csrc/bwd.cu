@@ -126,6 +126,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 // ---------------------------------------------------------------- preprocess
+// One padded row (bh, n) per D/8 threads, n < Npad: rows n >= N (the short last
+// block) get D = 0 and lse2 = +inf, so that their P is exactly 0.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                       const uint16_t* __restrict__ dout,
@@ -133,13 +135,17 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
                                                       float* __restrict__ delta,
                                                       float* __restrict__ lse2,
                                                       float* __restrict__ dq_accum,
-                                                      long long rows) {
+                                                      long long rows_pad, int N, int Npad) {
   constexpr int kThreadsPerRow = D / 8;  // 8 bf16 (16 bytes) per thread
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long row = gt / kThreadsPerRow;
+  const long long prow = gt / kThreadsPerRow;
   const int part = static_cast<int>(gt % kThreadsPerRow);
+  const long long bh = prow / Npad;
+  const int n = static_cast<int>(prow - bh * Npad);
+  const bool live = prow < rows_pad && n < N;
+  const long long row = bh * N + n;  // row of O, dO and LSE
   float acc = 0.f;
-  if (row < rows) {
+  if (live) {
     const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
     const uint4 g = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
     const uint32_t* ap = reinterpret_cast<const uint32_t*>(&a);
@@ -149,17 +155,19 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
       acc = fmaf(__uint_as_float(ap[i] << 16), __uint_as_float(gp[i] << 16), acc);
       acc = fmaf(__uint_as_float(ap[i] & 0xffff0000u), __uint_as_float(gp[i] & 0xffff0000u), acc);
     }
-    float4* z = reinterpret_cast<float4*>(dq_accum + row * D + part * 8);
+  }
+  if (prow < rows_pad) {
+    float4* z = reinterpret_cast<float4*>(dq_accum + prow * D + part * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int off = kThreadsPerRow / 2; off > 0; off >>= 1)
     acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && part == 0) {
-    delta[row] = acc;
-    const float L = lse[row];
-    lse2[row] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+  if (prow < rows_pad && part == 0) {
+    delta[prow] = acc;
+    const float L = live ? lse[row] : -INFINITY;
+    lse2[prow] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
   }
 }
 
@@ -247,8 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sDO + st * L::kTileBytes + ch * 16384, &mdo, ch * 64, q_row,
                       bar.q_full(st));
         }
-        bulk_load(smem_u32(lse_s + st * kTile), p.lse2 + q_row, kTile * 4, bar.q_full(st));
-        bulk_load(smem_u32(delta_s + st * kTile), p.delta + q_row, kTile * 4, bar.q_full(st));
+        // lse2 and D live in the padded [B*H, Npad] workspace arrays
+        const size_t prow = static_cast<size_t>(bh) * p.Npad + (list[t] >> 2) * kTile;
+        bulk_load(smem_u32(lse_s + st * kTile), p.lse2 + prow, kTile * 4, bar.q_full(st));
+        bulk_load(smem_u32(delta_s + st * kTile), p.delta + prow, kTile * 4, bar.q_full(st));
       }
     }
   } else if (warp == 13) {
@@ -325,9 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = (warp & 3) * 32 + lane;  // key within the block = TMEM lane
     const int key = kb * kTile + j;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const size_t col = static_cast<size_t>(bm) * p.N + key;
-    const int lts = p.mask.lts[col], lte = p.mask.lte[col];
-    const int uts = p.mask.uts ? p.mask.uts[col] : 0, ute = p.mask.ute ? p.mask.ute[col] : 0;
+    // keys >= N (the short last block of a sequence) do not exist: their P^T
+    // row is forced to 0 and their dK, dV rows are not stored
+    const bool key_exists = key < p.N;
+    const size_t col = static_cast<size_t>(bm) * p.N + (key_exists ? key : 0);
+    const int lts = key_exists ? p.mask.lts[col] : 0, lte = key_exists ? p.mask.lte[col] : 0;
+    const int uts = (key_exists && p.mask.uts) ? p.mask.uts[col] : 0;
+    const int ute = (key_exists && p.mask.ute) ? p.mask.ute[col] : 0;
     const bool causal = p.mask.causal != 0;
     const float c = p.scale_log2;
     bool ok = true;
@@ -352,7 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld64(a, a + 32, v);
         // masked-query bits of this thread's key column for queries 64g + [32h, 32h+32)
         uint32_t mb[2] = {0u, 0u};
-        if (lab == FM_TILE_PARTIAL) {
+        if (!key_exists) {
+          mb[0] = mb[1] = 0xffffffffu;
+        } else if (lab == FM_TILE_PARTIAL) {
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
             mb[hh] = column_mask_bits(key, lts, lte, uts, ute, causal,
@@ -448,7 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        store_row32_bf16(dst_row + ch * 32, v, f);
+        // every lane takes part in the (warp-collective) TMEM load; only
+        // existing keys store
+        if (key_exists) store_row32_bf16(dst_row + ch * 32, v, f);
       }
     }
   } else {
@@ -492,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t box = (ch * 16384 < L::kTileBytes)
                                    ? sQ + st * L::kTileBytes + ch * 16384
                                    : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
-          tma_reduce_add_2d(&mdq, box, ch * 32, head_row0 + qb * kTile);
+          tma_reduce_add_2d(&mdq, box, ch * 32, bh * p.Npad + qb * kTile);
         }
         bulk_commit_group();
         bulk_wait_read_all();  // the stage buffers may be refilled now
@@ -510,13 +528,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// dQ = bf16(scale * accumulator); 8 elements per thread of the unpadded
+// [heads, N, d] output, read from the padded [heads, Npad, d] accumulator.
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, float scale,
-                                                         uint16_t* __restrict__ dq,
-                                                         long long n8) {
+                                                         uint16_t* __restrict__ dq, long long n8,
+                                                         int N, int Npad, int d) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-  const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+  const long long e = i * 8;
+  const long long row = e / d;  // (bh, n) with n < N
+  const long long bh = row / N;
+  const long long src = (bh * Npad + (row - bh * N)) * d + (e - row * d);
+  const float4 a = *reinterpret_cast<const float4*>(acc + src);
+  const float4 b = *reinterpret_cast<const float4*>(acc + src + 4);
   uint4 o;
   o.x = pack_bf16x2(a.x * scale, a.y * scale);
   o.y = pack_bf16x2(a.z * scale, a.w * scale);
@@ -541,14 +565,16 @@ cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
-                           float* delta, float* lse2, float* dq_accum, long long rows,
-                           cudaStream_t s) {
-  const long long threads = rows * (d / 8);
+                           float* delta, float* lse2, float* dq_accum, long long heads, int N,
+                           int Npad, cudaStream_t s) {
+  const long long rows_pad = heads * Npad;
+  const long long threads = rows_pad * (d / 8);
   const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
   if (d == 64)
-    bwd_pre_kernel<64><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows);
+    bwd_pre_kernel<64><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows_pad, N, Npad);
   else
-    bwd_pre_kernel<128><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows);
+    bwd_pre_kernel<128><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows_pad, N,
+                                             Npad);
   return cudaGetLastError();
 }
 
@@ -560,11 +586,10 @@ cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, cons
 }
 
 cudaError_t launch_dq_convert(int d, const float* dq_accum, float scale, uint16_t* dq,
-                              long long elems, cudaStream_t s) {
-  (void)d;
-  const long long n8 = elems / 8;
+                              long long heads, int N, int Npad, cudaStream_t s) {
+  const long long n8 = heads * N * d / 8;
   const unsigned grid = static_cast<unsigned>((n8 + 255) / 256);
-  dq_convert_kernel<<<grid, 256, 0, s>>>(dq_accum, scale, dq, n8);
+  dq_convert_kernel<<<grid, 256, 0, s>>>(dq_accum, scale, dq, n8, N, Npad, d);
   return cudaGetLastError();
 }
 

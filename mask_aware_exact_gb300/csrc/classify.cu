@@ -14,14 +14,20 @@
 //    ranges of r, so the 128 columns of a key block add +1/-1 into two
 //    difference arrays over r; a prefix sum gives, per row block, how many
 //    columns cover it fully and how many touch it.
-//  * FULL iff all 128 columns cover the block fully; NONE iff no column
-//    touches it; otherwise PARTIAL.
+//  * FULL iff all columns of the key block cover the block fully; NONE iff no
+//    column touches it; otherwise PARTIAL.
+//  * N need not be a multiple of 128: the last blocks are short. Only rows and
+//    columns < N exist, so the label is exact over the existing entries; an
+//    interval that reaches row N covers the short last row block to its end,
+//    and columns >= N take no part (the attention kernels mask them).
 //
 // The same pass writes the per-key-block min/max of each vector, the labels in
 // both tile orders, the ascending lists of non-FULL tiles per key block and
 // (second kernel) per query block, and (third kernel) each block index ranked
 // by descending amount of work, which the attention kernels use as their
 // launch order (longest first).
+#include <climits>
+
 #include "internal.h"
 #include "flashmask.h"
 
@@ -66,16 +72,24 @@ __global__ void __launch_bounds__(128) classify_cols_kernel(MaskDev m, int N, in
 
   const size_t base = static_cast<size_t>(bm) * N;
   const int j = c * kTile + tid;
-  int v[4];
-  v[0] = m.lts[base + j];
-  v[1] = m.lte[base + j];
-  v[2] = m.uts ? m.uts[base + j] : 0;
-  v[3] = m.ute ? m.ute[base + j] : 0;
+  const bool exists = j < N;                 // the last key block may be short
+  const int ncols = min(kTile, N - c * kTile);
+  const int Npad = Tr * kTile;
+  int v[4] = {0, 0, 0, 0};
+  if (exists) {
+    v[0] = m.lts[base + j];
+    v[1] = m.lte[base + j];
+    v[2] = m.uts ? m.uts[base + j] : 0;
+    v[3] = m.ute ? m.ute[base + j] : 0;
+  }
 
   // per-key-block min / max of each vector
   int mm[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) mm[2 * k] = mm[2 * k + 1] = v[k];
+  for (int k = 0; k < 4; ++k) {
+    mm[2 * k] = exists ? v[k] : INT_MAX;
+    mm[2 * k + 1] = exists ? v[k] : INT_MIN;
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
@@ -95,20 +109,23 @@ __global__ void __launch_bounds__(128) classify_cols_kernel(MaskDev m, int N, in
     t.minmax[(static_cast<size_t>(bm) * Tc + c) * 8 + tid] = r;
   }
 
-  // masked row intervals of column j, clamped to [0, N]
+  // masked row intervals of column j, clamped to [0, N]; an end at N is
+  // extended to the padded row count so that it covers the short last block
   int s[3], e[3], n = 0;
   auto add = [&](int a0, int a1) {
     a0 = max(a0, 0);
     a1 = min(a1, N);
     if (a0 < a1) {
       s[n] = a0;
-      e[n] = a1;
+      e[n] = a1 == N ? Npad : a1;
       ++n;
     }
   };
-  if (m.causal) add(0, j);
-  add(v[0], v[1]);
-  add(v[2], v[3]);
+  if (exists) {
+    if (m.causal) add(0, j);
+    add(v[0], v[1]);
+    add(v[2], v[3]);
+  }
   // sort by start (at most three)
   for (int a = 0; a < n; ++a)
     for (int b = a + 1; b < n; ++b)
@@ -151,7 +168,7 @@ __global__ void __launch_bounds__(128) classify_cols_kernel(MaskDev m, int N, in
     carry_full += tot;
     const int tc = block_scan128(td, warp_tot, tot) + carry_touch;
     carry_touch += tot;
-    const int lab = (fc == kTile) ? FM_TILE_FULL : (tc == 0 ? FM_TILE_NONE : FM_TILE_PARTIAL);
+    const int lab = (fc == ncols) ? FM_TILE_FULL : (tc == 0 ? FM_TILE_NONE : FM_TILE_PARTIAL);
     const int keep = (r < Tr && lab != FM_TILE_FULL) ? 1 : 0;
     const int pos = block_scan128(keep, warp_tot, tot) - keep + carry_cnt;
     carry_cnt += tot;
@@ -210,7 +227,7 @@ __global__ void __launch_bounds__(256) classify_order_kernel(int Tr, int Tc, Cla
 
 cudaError_t launch_classify(const MaskDev& m, int B, int N, const ClassifyTables& t,
                             cudaStream_t s) {
-  const int Tr = N / kTile, Tc = Tr;
+  const int Tr = (N + kTile - 1) / kTile, Tc = Tr;
   const int BHm = B * m.Hm;
   const size_t sh_cols = static_cast<size_t>(2) * (Tr + 1) * sizeof(int);
   const size_t sh_order = static_cast<size_t>(Tr) * sizeof(int);

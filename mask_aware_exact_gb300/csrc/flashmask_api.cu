@@ -14,12 +14,16 @@ using fm::kTile;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Blocks per sequence and the per-head row count of the padded workspace arrays
+// (the last block of a sequence whose length is not a multiple of 128 is short).
+int blocks_of(int N) { return (N + kTile - 1) / kTile; }
+int padded(int N) { return blocks_of(N) * kTile; }
+
 bool shape_ok(int B, int H, int Hm, int N, int d) {
   if (B <= 0 || H <= 0 || Hm <= 0 || N <= 0) return false;
   if (d != 64 && d != 128) return false;
-  if (N % kTile != 0) return false;
   if (H % Hm != 0) return false;
-  const long long rows = static_cast<long long>(B) * H * N;
+  const long long rows = static_cast<long long>(B) * H * padded(N);
   if (rows >= (1LL << 31)) return false;
   return true;
 }
@@ -27,8 +31,8 @@ bool shape_ok(int B, int H, int Hm, int N, int d) {
 fm_ws_layout make_layout(int B, int H, int Hm, int N, int d, int for_bwd) {
   fm_ws_layout L;
   std::memset(&L, 0, sizeof(L));
-  const size_t Tr = N / kTile, Tc = Tr, BHm = static_cast<size_t>(B) * Hm;
-  const size_t BHN = static_cast<size_t>(B) * H * N;
+  const size_t Tr = blocks_of(N), Tc = Tr, BHm = static_cast<size_t>(B) * Hm;
+  const size_t BHN = static_cast<size_t>(B) * H * padded(N);  // padded rows per head
   size_t off = 0;
   L.status = off;
   off = align_up(off + 16, 256);
@@ -207,8 +211,8 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
   p.B = B;
   p.H = H;
   p.N = N;
-  p.Tr = N / kTile;
-  p.Tc = N / kTile;
+  p.Tr = blocks_of(N);
+  p.Tc = blocks_of(N);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.row_count = t.row_count;
   p.row_list = t.row_list;
@@ -228,11 +232,11 @@ fm_status flashmask_bwd_preprocess(const void* o, const float* lse, const void* 
   const fm_status ws_st = check_ws(ws, ws_bytes, L);
   if (ws_st != FM_OK) return ws_st;
   char* w = static_cast<char*>(ws);
-  const long long rows = static_cast<long long>(B) * H * N;
   return fm::launch_bwd_pre(d, static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
                             lse, reinterpret_cast<float*>(w + L.delta),
                             reinterpret_cast<float*>(w + L.lse2),
-                            reinterpret_cast<float*>(w + L.dq_accum), rows,
+                            reinterpret_cast<float*>(w + L.dq_accum),
+                            static_cast<long long>(B) * H, N, padded(N),
                             static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FM_OK
              : FM_ERR_CUDA;
@@ -251,11 +255,12 @@ fm_status flashmask_bwd_main(const void* q, const void* k, const void* v, const 
   const fm_status ws_st = check_ws(ws, ws_bytes, L);
   if (ws_st != FM_OK) return ws_st;
   const long long rows = static_cast<long long>(B) * H * N;
+  const long long rows_pad = static_cast<long long>(B) * H * padded(N);
   char* w = static_cast<char*>(ws);
   float* dq_accum = reinterpret_cast<float*>(w + L.dq_accum);
   CUtensorMap mq, mk, mv, mdo, mdq;
   if (!make_map(&mq, q, rows, d) || !make_map(&mk, k, rows, d) || !make_map(&mv, v, rows, d) ||
-      !make_map(&mdo, dout, rows, d) || !make_map_f32(&mdq, dq_accum, rows, d))
+      !make_map(&mdo, dout, rows, d) || !make_map_f32(&mdq, dq_accum, rows_pad, d))
     return FM_ERR_CUDA;
   const fm::ClassifyTables t = tables(L, ws);
   fm::BwdParams p;
@@ -263,8 +268,9 @@ fm_status flashmask_bwd_main(const void* q, const void* k, const void* v, const 
   p.B = B;
   p.H = H;
   p.N = N;
-  p.Tr = N / kTile;
-  p.Tc = N / kTile;
+  p.Npad = padded(N);
+  p.Tr = blocks_of(N);
+  p.Tc = blocks_of(N);
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.col_count = t.col_count;
@@ -290,10 +296,9 @@ fm_status flashmask_bwd_finalize(int B, int H, int Hm, int N, int d, float scale
   const fm_ws_layout L = make_layout(B, H, Hm, N, d, 1);
   const fm_status ws_st = check_ws(ws, ws_bytes, L);
   if (ws_st != FM_OK) return ws_st;
-  const long long elems = static_cast<long long>(B) * H * N * d;
   return fm::launch_dq_convert(d, reinterpret_cast<const float*>(static_cast<char*>(ws) + L.dq_accum),
-                               scale, static_cast<uint16_t*>(dq), elems,
-                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+                               scale, static_cast<uint16_t*>(dq), static_cast<long long>(B) * H, N,
+                               padded(N), static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FM_OK
              : FM_ERR_CUDA;
 }

@@ -117,10 +117,11 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, float f) {
   }
 }
 
-// Writes kOCols (16 or 32) TMEM columns of this lane's row, times f, as bf16.
+// Writes n (16 or 32) TMEM columns of this lane's row, times f, as bf16 (the TMEM
+// load runs on every lane of the warp; only lanes with `store` write).
 template <int n>
 __device__ __forceinline__ void tmem_cols_to_bf16(uint32_t taddr, bool live, float f,
-                                                  uint16_t* dst) {
+                                                  uint16_t* dst, bool store) {
   uint32_t v[n];
   if (live) {
     if constexpr (n == 32) {
@@ -132,6 +133,7 @@ __device__ __forceinline__ void tmem_cols_to_bf16(uint32_t taddr, bool live, flo
 #pragma unroll
     for (int i = 0; i < n; ++i) v[i] = 0u;
   }
+  if (!store) return;  // after the (warp-collective) TMEM load
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < n / 8; ++i) {
@@ -322,22 +324,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int entry = next_entry;
       if (j + 1 < ntiles) next_entry = list[j + 1];
       const int g = j % kSRegions;
-      const bool partial = (entry & 3) == FM_TILE_PARTIAL;
-      // PARTIAL tile: lane l builds the masked-row bits of key column
-      // 64w + 32k + l for this warp's 32 rows; a bit transpose hands each lane
-      // its own row's bits over those 32 columns. The bound loads overlap the
-      // wait for S.
+      // The element mask applies on PARTIAL tiles and on every tile of a short
+      // last key block (its keys >= N do not exist and are masked).
+      const bool short_keys = (entry >> 2) * kTile + kTile > p.N;
+      const bool partial = (entry & 3) == FM_TILE_PARTIAL || short_keys;
+      // lane l builds the masked-row bits of key column 64w + 32k + l for this
+      // warp's 32 rows; a bit transpose hands each lane its own row's bits
+      // over those 32 columns. The bound loads overlap the wait for S.
       uint32_t mbits[2] = {0u, 0u};
       if (partial) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int jc = (entry >> 2) * kTile + 64 * w + 32 * k + lane;
-          const size_t col = static_cast<size_t>(bm) * p.N + jc;
-          const int lts = p.mask.lts[col], lte = p.mask.lte[col];
-          const int uts = p.mask.uts ? p.mask.uts[col] : 0, ute = p.mask.ute ? p.mask.ute[col] : 0;
-          mbits[k] = warp_transpose_bits(column_mask_bits(jc, lts, lte, uts, ute,
-                                                          p.mask.causal != 0,
-                                                          r * kTile + 32 * (warp & 3)));
+          uint32_t colbits = 0xffffffffu;  // a key >= N masks every row
+          if (jc < p.N) {
+            const size_t col = static_cast<size_t>(bm) * p.N + jc;
+            const int lts = p.mask.lts[col], lte = p.mask.lte[col];
+            const int uts = p.mask.uts ? p.mask.uts[col] : 0;
+            const int ute = p.mask.ute ? p.mask.ute[col] : 0;
+            colbits = column_mask_bits(jc, lts, lte, uts, ute, p.mask.causal != 0,
+                                       r * kTile + 32 * (warp & 3));
+          }
+          mbits[k] = warp_transpose_bits(colbits);
         }
       }
       if (ok) {
@@ -430,12 +438,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = ok && ntiles > 0;
     const bool has = live && ltot > 0.f;
     const float inv = has ? 1.f / ltot : 0.f;
+    // rows >= N of a short last query block do not exist: nothing is stored
+    const bool row_exists = r * kTile + row < p.N;
     uint16_t* orow = p.o + static_cast<size_t>(q_row0 + row) * D + w * kOCols;
 #pragma unroll
     for (int ch = 0; ch < kOCols / 32; ++ch)
       tmem_cols_to_bf16<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, live, inv,
-                            orow + 32 * ch);
-    if (w == 0) {
+                            orow + 32 * ch, row_exists);
+    if (w == 0 && row_exists) {
       const float m_fin = (m == -INFINITY) ? 0.f : m;
       p.lse[q_row0 + row] = has ? (m_fin + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
     }

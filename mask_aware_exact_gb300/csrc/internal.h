@@ -56,14 +56,15 @@ struct FwdParams {
 struct BwdParams {
   MaskDev mask;
   int B, H, N, Tr, Tc;
+  int Npad;          // rows per head of lse2, delta and dq_accum (Tr * 128)
   float scale;       // applied to dK here and to dQ in the conversion kernel
   float scale_log2;  // scale * log2(e)
   const int32_t* col_count;
   const int32_t* col_list;
   const int32_t* col_order;
-  const float* lse2;   // [B,H,N]
-  const float* delta;  // [B,H,N]
-  float* dq_accum;     // [B,H,N,d]
+  const float* lse2;   // [B,H,Npad]
+  const float* delta;  // [B,H,Npad]
+  float* dq_accum;     // [B,H,Npad,d]
   uint16_t* dk;
   uint16_t* dv;
   int32_t* status;
@@ -74,12 +75,12 @@ cudaError_t launch_classify(const MaskDev& m, int B, int N, const ClassifyTables
 cudaError_t launch_fwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const FwdParams& p, cudaStream_t s);
 cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
-                           float* delta, float* lse2, float* dq_accum, long long rows,
-                           cudaStream_t s);
+                           float* delta, float* lse2, float* dq_accum, long long heads, int N,
+                           int Npad, cudaStream_t s);
 cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
                        cudaStream_t s);
 cudaError_t launch_dq_convert(int d, const float* dq_accum, float scale, uint16_t* dq,
-                              long long elems, cudaStream_t s);
+                              long long heads, int N, int Npad, cudaStream_t s);
 
 }  // namespace fm

@@ -244,7 +244,7 @@ def flashmask_status_string(status: int) -> str:
 def read_classification(ws: torch.Tensor, B: int, Hm: int, N: int) -> dict:
     """Copies the classification regions of a workspace to host numpy arrays."""
     L = flashmask_workspace_layout(B, Hm, Hm, N, 64, False)
-    Tr = Tc = N // FM_TILE
+    Tr = Tc = (N + FM_TILE - 1) // FM_TILE
     h = ws[:L.total].cpu().numpy()
 
     def region(off, count, dtype, shape):

@@ -47,9 +47,14 @@ def test_workspace_sizes(lib):
     BHN = 32 * 32768
     assert b - f >= BHN * 4 * 2 + BHN * 128 * 4
     assert f >= 256 * 256 * 2  # two label tables
-    for bad in [(1, 32, 1, 32768, 96), (1, 32, 1, 1000, 128), (1, 32, 3, 1024, 128),
-                (0, 1, 1, 128, 64), (1, 1, 1, 0, 64)]:
+    for bad in [(1, 32, 1, 32768, 96), (1, 32, 3, 1024, 128), (0, 1, 1, 128, 64),
+                (1, 1, 1, 0, 64), (1, 1, 1, -128, 64)]:
         assert fm.flashmask_workspace_bytes(*bad, True) == 0
+    # a sequence length that is not a multiple of 128: the tables cover
+    # ceil(N / 128) blocks and the backward arrays are padded to 128 rows
+    L = fm.flashmask_workspace_layout(1, 2, 1, 1000, 64, True)
+    assert L.total - L.dq_accum == 2 * 1024 * 64 * 4
+    assert L.labels_t - L.labels >= 8 * 8
 
 
 def test_workspace_layout_regions_disjoint(lib):
@@ -79,7 +84,7 @@ def test_fwd_argument_errors(lib):
     assert call_fwd(lib, scale=float("nan")) == fm.FM_ERR_INVALID_ARG
     assert call_fwd(lib, scale=-1.0) == fm.FM_ERR_INVALID_ARG
     assert call_fwd(lib, d=96) == fm.FM_ERR_UNSUPPORTED
-    assert call_fwd(lib, N=200) == fm.FM_ERR_UNSUPPORTED
+    assert call_fwd(lib, N=0) == fm.FM_ERR_UNSUPPORTED
     assert call_fwd(lib, H=3, Hm=2) == fm.FM_ERR_UNSUPPORTED
     assert call_fwd(lib, ws=None) == fm.FM_ERR_WORKSPACE
     assert call_fwd(lib, ws=FAKE + 16) == fm.FM_ERR_WORKSPACE
@@ -102,7 +107,7 @@ def test_bwd_and_classify_argument_errors(lib):
                            FAKE, FAKE, 1 << 30, 0, None)
     assert st == fm.FM_ERR_INVALID_ARG
     assert lib.flashmask_classify(None, 1, 256, FAKE, 1 << 30, None) == fm.FM_ERR_INVALID_ARG
-    assert lib.flashmask_classify(ctypes.byref(m), 1, 250, FAKE, 1 << 30, None) == fm.FM_ERR_UNSUPPORTED
+    assert lib.flashmask_classify(ctypes.byref(m), 1, 0, FAKE, 1 << 30, None) == fm.FM_ERR_UNSUPPORTED
     assert lib.flashmask_classify(ctypes.byref(m), 1, 256, FAKE, 8, None) == fm.FM_ERR_WORKSPACE
     assert lib.flashmask_workspace_layout(1, 2, 1, 256, 64, 1, None) == fm.FM_ERR_INVALID_ARG
     assert lib.flashmask_check_status(None, None, None) == fm.FM_ERR_WORKSPACE

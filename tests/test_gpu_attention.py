@@ -182,3 +182,24 @@ def test_window_prefix_reduced_full():
     spec = W.window_prefix_bounds(B, 1, N, 4096, 2048)
     q, k, v, do = W.make_qkv(B, H, N, d, seed=0)
     full_compare(fm, q, k, v, do, spec, what="window_prefix N=8192")
+
+
+@pytest.mark.parametrize("N,d,kind", [(129, 64, "causal"), (200, 128, "document"),
+                                      (333, 64, "random"), (600, 128, "window_prefix"),
+                                      (1000, 128, "share_question"), (77, 128, "random")])
+def test_ragged_sequence_lengths(N, d, kind):
+    # N not a multiple of 128: short last query and key blocks, compared in full
+    fm = need_gpu()
+    B, H = 2, 2
+    if kind == "causal":
+        spec = W.causal_bounds(B, 1, N)
+    elif kind == "document":
+        spec = W.document_bounds(B, 1, [61, 100, 39])
+    elif kind == "window_prefix":
+        spec = W.window_prefix_bounds(B, 1, N, 150, 70)
+    elif kind == "share_question":
+        spec = W.share_question_bounds(B, 1, 300, [250, 290, 160])
+    else:
+        spec = W.random_bounds(B, 2, N, causal=N % 2 == 1, seed=N, upper=True)
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=N)
+    full_compare(fm, q, k, v, do, spec, what=f"ragged N={N} {kind} d={d}")

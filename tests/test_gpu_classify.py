@@ -109,3 +109,20 @@ def test_classify_extreme_bounds():
     c = gpu_classify(fm, spec)
     assert np.array_equal(c["labels"][0, 0], oracle_labels(spec, 0, 0))
     assert np.array_equal(c["minmax"][0, 0], oracle_minmax(spec, 0, 0))
+
+
+@pytest.mark.parametrize("N,seed", [(130, 0), (300, 1), (777, 2), (1000, 3), (64, 4), (1, 5)])
+def test_classify_ragged_lengths(N, seed):
+    # N not a multiple of 128: the last row and key blocks are short and the
+    # labels are exact over the entries that exist
+    fm = need_gpu()
+    B, Hm = 1 + seed % 2, 1 + seed % 3
+    spec = W.random_bounds(B, Hm, N, causal=seed % 2 == 0, seed=500 + seed, upper=True)
+    c = gpu_classify(fm, spec)
+    Tr = (N + 127) // 128
+    assert c["labels"].shape[-1] == Tr
+    for b in range(B):
+        for hm in range(Hm):
+            assert np.array_equal(c["labels"][b, hm], oracle_labels(spec, b, hm))
+            assert np.array_equal(c["minmax"][b, hm], oracle_minmax(spec, b, hm))
+            check_consistency(c, b, hm)

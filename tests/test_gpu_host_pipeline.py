@@ -29,12 +29,13 @@ CASES = [
     (2, 4, 2, 384, 64, (1, 2, 4), "random"),
     (1, 6, 3, 640, 128, (2, 6), "document"),
     (1, 2, 1, 256, 64, (1, 2), "workload0"),
+    (2, 4, 1, 333, 128, (2,), "random"),
 ]
 
 
 def make_spec(kind, B, Hm, N):
     if kind == "random":
-        return W.random_bounds(B, Hm, N, causal=True, seed=77, upper=True)
+        return W.random_bounds(B, Hm, N, causal=True, seed=77 + N, upper=True)
     if kind == "document":
         lengths = [200, 37, 300, 103]
         spec = W.document_bounds(B, 1, lengths)

@@ -28,7 +28,8 @@ def test_host_workspace_bytes(lib):
     assert fm.flashmask_host_workspace_bytes(1, 6, 3, 1024, 64, 3) == 0   # groups of 2, chunk 3
     assert fm.flashmask_host_workspace_bytes(1, 6, 3, 1024, 64, 2) > 0
     assert fm.flashmask_host_workspace_bytes(1, 6, 3, 1024, 64, 6) > 0
-    assert fm.flashmask_host_workspace_bytes(1, 6, 3, 1000, 64, 2) == 0   # N % 128
+    assert fm.flashmask_host_workspace_bytes(1, 6, 3, 0, 64, 2) == 0      # N
+    assert fm.flashmask_host_workspace_bytes(1, 6, 3, 1000, 64, 2) > 0    # ragged N
     assert fm.flashmask_host_workspace_bytes(1, 6, 3, 1024, 96, 2) == 0   # d
 
 
