@@ -203,6 +203,29 @@ fm_status flashmask_fwd_bwd_host(const void* q, const void* k, const void* v, co
                                  void* o, float* lse, void* dq, void* dk, void* dv, void* dev_ws,
                                  size_t ws_bytes, int chunk_heads, void* stream);
 
+/* Per-rank mask localisation for context parallelism ("FlashMask-3: ... Mask-Aware
+ * Distributed Attention", abstract: under any multi-chunk context-parallel
+ * assignment, per-rank localisation reduces to a zero-communication
+ * clip-shift-max on the boundary vectors). For a rank that holds the query rows
+ * [row0, row0 + rows) of each sequence and every key, writes the boundary
+ * vectors of its local problem: int32 [B, Hm, N] device arrays lts, lte, uts,
+ * ute (all four written; caller-owned) in local row coordinates [0, rows),
+ * with no causal flag (the local mask is non-causal):
+ *   every bound b -> min(max(b - row0, 0), rows)               (clip, shift)
+ *   causal: key j's masked rows [0, j) become [0, c), c = clip(j - row0), and
+ *   join the upper interval as [0, max(c, end))                 (max)
+ * Column j of the local mask then marks exactly the chunk's rows that the
+ * global mask marks, whenever that upper interval is empty or starts at a row
+ * <= c (true for every causal mask whose upper interval lies above the
+ * diagonal). Otherwise the column masks more than it should and *inexact
+ * (device int32, may be NULL; set to 1, never cleared) records it. A rank with
+ * several chunks calls this once per chunk. Keys are not localised (the local
+ * problem is rows x N). Bad arguments (row0 < 0, rows < 1, row0 + rows > N,
+ * null pointers) return before any launch. Asynchronous on `stream`. */
+fm_status flashmask_localize(const fm_mask* mask, int B, int N, int row0, int rows, int32_t* lts,
+                             int32_t* lte, int32_t* uts, int32_t* ute, int32_t* inexact,
+                             void* stream);
+
 /* Synchronises `stream`, then reads and clears the workspace status word.
  * Returns FM_ERR_TIMEOUT if a kernel wait gave up since the last check,
  * FM_ERR_CUDA if the stream reports an error, FM_OK otherwise. If detail is

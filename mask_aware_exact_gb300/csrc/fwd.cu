@@ -146,7 +146,7 @@ __device__ __forceinline__ void tmem_cols_to_bf16(uint32_t taddr, bool live, flo
   }
 }
 
-template <int D>
+template <int D, bool kShortLast>  // kShortLast: N is not a multiple of 128
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const FwdParams p) {
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = j % kSRegions;
       // The element mask applies on PARTIAL tiles and on every tile of a short
       // last key block (its keys >= N do not exist and are masked).
-      const bool short_keys = (entry >> 2) * kTile + kTile > p.N;
+      const bool short_keys = kShortLast && (entry >> 2) == p.Tc - 1;
       const bool partial = (entry & 3) == FM_TILE_PARTIAL || short_keys;
       // lane l builds the masked-row bits of key column 64w + 32k + l for this
       // warp's 32 rows; a bit transpose hands each lane its own row's bits
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 2; ++k) {
           const int jc = (entry >> 2) * kTile + 64 * w + 32 * k + lane;
           uint32_t colbits = 0xffffffffu;  // a key >= N masks every row
-          if (jc < p.N) {
+          if (!kShortLast || jc < p.N) {
             const size_t col = static_cast<size_t>(bm) * p.N + jc;
             const int lts = p.mask.lts[col], lte = p.mask.lte[col];
             const int uts = p.mask.uts ? p.mask.uts[col] : 0;
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool has = live && ltot > 0.f;
     const float inv = has ? 1.f / ltot : 0.f;
     // rows >= N of a short last query block do not exist: nothing is stored
-    const bool row_exists = r * kTile + row < p.N;
+    const bool row_exists = !kShortLast || r * kTile + row < p.N;
     uint16_t* orow = p.o + static_cast<size_t>(q_row0 + row) * D + w * kOCols;
 #pragma unroll
     for (int ch = 0; ch < kOCols / 32; ++ch)
@@ -459,15 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kShortLast>
 cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const FwdParams& p, cudaStream_t s) {
   using L = FwdLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::kBytes);
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kShortLast>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.B * p.H * p.Tr);
-  fwd_kernel<D><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, p);
+  fwd_kernel<D, kShortLast><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -475,8 +475,12 @@ cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 
 cudaError_t launch_fwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const FwdParams& p, cudaStream_t s) {
-  if (d == 64) return launch_fwd_t<64>(mq, mk, mv, p, s);
-  return launch_fwd_t<128>(mq, mk, mv, p, s);
+  const bool short_last = p.N % kTile != 0;
+  if (d == 64)
+    return short_last ? launch_fwd_t<64, true>(mq, mk, mv, p, s)
+                      : launch_fwd_t<64, false>(mq, mk, mv, p, s);
+  return short_last ? launch_fwd_t<128, true>(mq, mk, mv, p, s)
+                    : launch_fwd_t<128, false>(mq, mk, mv, p, s);
 }
 
 }  // namespace fm

@@ -39,7 +39,8 @@ class FmWsLayout(ctypes.Structure):
 EXPORTED = ("flashmask_workspace_bytes", "flashmask_workspace_layout", "flashmask_classify",
             "flashmask_fwd", "flashmask_bwd", "flashmask_bwd_preprocess", "flashmask_bwd_main",
             "flashmask_bwd_finalize", "flashmask_fwd_noalloc", "flashmask_host_workspace_bytes",
-            "flashmask_fwd_bwd_host", "flashmask_check_status", "flashmask_status_string")
+            "flashmask_fwd_bwd_host", "flashmask_localize", "flashmask_check_status",
+            "flashmask_status_string")
 
 _lib = None
 
@@ -80,6 +81,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.flashmask_fwd_bwd_host.argtypes = [vp, vp, vp, vp, ctypes.POINTER(_FmMask), i, i, i, i, f, vp,
                                          vp, vp, vp, vp, vp, sz, i, vp]
     L.flashmask_fwd_bwd_host.restype = i
+    L.flashmask_localize.argtypes = [ctypes.POINTER(_FmMask), i, i, i, i, vp, vp, vp, vp, vp, vp]
+    L.flashmask_localize.restype = i
     L.flashmask_check_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     L.flashmask_check_status.restype = i
     L.flashmask_status_string.argtypes = [i]
@@ -352,3 +355,18 @@ def flashmask_fwd_bwd_host(q, k, v, do, mask: HostMask, dev_ws, chunk_heads, sca
                                          dev_ws.data_ptr(), dev_ws.numel(), int(chunk_heads),
                                          _stream_ptr(stream)), "flashmask_fwd_bwd_host")
     return o, lse, dq, dk, dv
+
+
+def flashmask_localize(mask: DeviceMask, B: int, N: int, row0: int, rows: int, stream=None):
+    """Boundary vectors of the local problem of a rank holding query rows
+    [row0, row0 + rows): returns (DeviceMask with causal=False, inexact flag as
+    a bool). Synchronises the stream to read the flag."""
+    dev = mask.lts.device
+    shape = (B, mask.Hm, N)
+    out = [torch.empty(shape, dtype=torch.int32, device=dev) for _ in range(4)]
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    m = mask.c_struct()
+    _check(load().flashmask_localize(ctypes.byref(m), B, N, int(row0), int(rows), out[0].data_ptr(),
+                                     out[1].data_ptr(), out[2].data_ptr(), out[3].data_ptr(),
+                                     flag.data_ptr(), _stream_ptr(stream)), "flashmask_localize")
+    return DeviceMask(out[0], out[1], out[2], out[3], False), bool(flag.item())

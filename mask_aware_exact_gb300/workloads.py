@@ -154,6 +154,56 @@ def window_prefix_bounds(B: int, Hm: int, N: int, window: int, prefix: int) -> M
                     {"window": window, "prefix": prefix})
 
 
+def bidirectional_document_bounds(B: int, Hm: int, lengths: list[int]) -> MaskSpec:
+    """Full (non-causal) attention within packed documents, causal=False: a key
+    in the document [s, e) is masked for rows before the document (upper
+    interval [0, s)) and rows after it (lower interval [e, N))."""
+    N = int(sum(lengths))
+    lts = np.empty(N, dtype=np.int32)
+    ute = np.empty(N, dtype=np.int32)
+    s = 0
+    for L in lengths:
+        lts[s:s + L] = s + L
+        ute[s:s + L] = s
+        s += L
+    bc = lambda a: np.broadcast_to(a, (B, Hm, N)).copy()
+    lte = np.full(N, N, dtype=np.int32)
+    uts = np.zeros(N, dtype=np.int32)
+    return MaskSpec("bidirectional_document", False, bc(lts), bc(lte), bc(uts), bc(ute),
+                    {"lengths": list(lengths)})
+
+
+def block_causal_bounds(B: int, Hm: int, N: int, block: int) -> MaskSpec:
+    """Causal at block granularity (a block-sparse pattern), causal=False: a key
+    in block c = j // block is masked for the rows of earlier blocks (upper
+    interval [0, c * block)) and seen by every row from its block on."""
+    j = np.arange(N, dtype=np.int64)
+    ute = ((j // block) * block).astype(np.int32)
+    bc = lambda a: np.broadcast_to(a, (B, Hm, N)).copy()
+    lts = np.full(N, N, dtype=np.int32)
+    return MaskSpec("block_causal", False, bc(lts), bc(lts.copy()), bc(np.zeros(N, np.int32)),
+                    bc(ute), {"block": block})
+
+
+def stack_heads(specs: list[MaskSpec]) -> MaskSpec:
+    """One mask per head (Hm = len(specs)): the specs' [B, 1, N] vectors side by
+    side. All must share B, N and the causal flag; a spec without an upper
+    interval contributes an empty one."""
+    causal = specs[0].causal
+    assert all(s.causal == causal for s in specs)
+    def up(s, which):
+        v = getattr(s, which)
+        if v is not None:
+            return v
+        return np.zeros_like(s.lts)
+    any_upper = any(s.uts is not None for s in specs)
+    cat = lambda name: np.concatenate([getattr(s, name) for s in specs], axis=1)
+    uts = np.concatenate([up(s, "uts") for s in specs], axis=1) if any_upper else None
+    ute = np.concatenate([up(s, "ute") for s in specs], axis=1) if any_upper else None
+    return MaskSpec("per_head", causal, cat("lts"), cat("lte"), uts, ute,
+                    {"families": [s.family for s in specs]})
+
+
 def random_bounds(B: int, Hm: int, N: int, causal: bool, seed: int, upper: bool = True) -> MaskSpec:
     """Adversarial bounds for fuzzing: values anywhere in [-8, N+8], empty and
     reversed intervals, intervals touching 0 and N, overlapping LT/UT."""

@@ -33,6 +33,20 @@ def causal_document(lengths, rows=None) -> np.ndarray:
     return (doc[r][:, None] == doc[None, :]) & (j <= i)
 
 
+def bidirectional_document(lengths, rows=None) -> np.ndarray:
+    """Row i sees key j iff both lie in the same document (no causal order)."""
+    doc = _doc_ids(lengths)
+    N = len(doc)
+    _, _, r = _ij(N, rows)
+    return doc[r][:, None] == doc[None, :]
+
+
+def block_causal(N: int, block: int, rows=None) -> np.ndarray:
+    """Row i sees key j iff j's block is not after i's block."""
+    i, j, _ = _ij(N, rows)
+    return (j // block) <= (i // block)
+
+
 def share_question(q_len: int, answers, rows=None) -> np.ndarray:
     """Question rows see the question causally; an answer row sees the whole
     question before it and its own answer causally, never another answer."""

@@ -203,3 +203,43 @@ def test_ragged_sequence_lengths(N, d, kind):
         spec = W.random_bounds(B, 2, N, causal=N % 2 == 1, seed=N, upper=True)
     q, k, v, do = W.make_qkv(B, H, N, d, seed=N)
     full_compare(fm, q, k, v, do, spec, what=f"ragged N={N} {kind} d={d}")
+
+
+@pytest.mark.parametrize("kind,N,d", [("bidirectional_document", 640, 128),
+                                      ("bidirectional_document", 300, 64),
+                                      ("block_causal", 640, 64), ("block_causal", 500, 128),
+                                      ("per_head", 384, 128)])
+def test_more_mask_families(kind, N, d):
+    fm = need_gpu()
+    B = 2
+    if kind == "bidirectional_document":
+        lengths = [N // 3, N // 4, N - N // 3 - N // 4]
+        spec, H = W.bidirectional_document_bounds(B, 1, lengths), 2
+    elif kind == "block_causal":
+        spec, H = W.block_causal_bounds(B, 1, N, 96), 2
+    else:
+        # one mask per head (Hm = H = 4), four families with one causal flag
+        parts = [W.document_bounds(B, 1, [100, 200, 84]), W.causal_bounds(B, 1, N),
+                 W.share_question_bounds(B, 1, 128, [128, 128]),
+                 W.random_bounds(B, 1, N, causal=True, seed=9, upper=True)]
+        spec, H = W.stack_heads(parts), 4
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=N + d)
+    full_compare(fm, q, k, v, do, spec, what=f"{kind} N={N} d={d}")
+
+
+def test_classification_reused_across_layers():
+    # one classification of the mask serves several forward calls (layers of a
+    # model that share the mask), each with its own Q, K, V
+    fm = need_gpu()
+    B, H, N, d = 1, 4, 512, 128
+    spec = W.document_bounds(B, 2, [200, 312])  # Hm = 2: two heads per mask head
+    mask = fm.DeviceMask.from_spec(spec)
+    ws = fm.alloc_workspace(B, H, mask.Hm, N, d, for_bwd=False)
+    fm.flashmask_classify(mask, B, N, ws)
+    for layer in range(3):
+        q, k, v, _ = W.make_qkv(B, H, N, d, seed=40 + layer)
+        o, lse = fm.flashmask_fwd(q.cuda(), k.cuda(), v.cuda(), mask, ws, ws_classified=True)
+        o_ref, lse_ref = A.forward(q, k, v, spec, 1 / math.sqrt(d))
+        check_forward(to_np(o), to_np(lse), o_ref, lse_ref, f"layer {layer}")
+    st, site = fm.flashmask_check_status(ws)
+    assert st == fm.FM_OK, (st, site)

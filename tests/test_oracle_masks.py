@@ -108,3 +108,25 @@ def test_decoded_count_matches_closed_form_small():
     w = W.workload(0)
     m = w.mask
     assert visible_count(w.N, m.lts[0, 0], m.lte[0, 0], None, None, True) == 15631
+
+
+@pytest.mark.parametrize("lengths", [[5, 7, 1, 20], [100, 28], [300, 37, 129, 1]])
+def test_bidirectional_document(lengths):
+    spec = W.bidirectional_document_bounds(1, 1, lengths)
+    compare_blocked(spec, lambda r: MI.bidirectional_document(lengths, r), block=64)
+
+
+@pytest.mark.parametrize("N,block", [(256, 128), (333, 128), (200, 64), (100, 7)])
+def test_block_causal(N, block):
+    spec = W.block_causal_bounds(1, 1, N, block)
+    compare_blocked(spec, lambda r: MI.block_causal(N, block, r), block=64)
+
+
+def test_stack_heads_decodes_each_head():
+    # per-head masks: head hm of the stack decodes to the hm-th family's mask
+    N = 200
+    parts = [W.document_bounds(1, 1, [120, 80]), W.causal_bounds(1, 1, N)]
+    spec = W.stack_heads(parts)
+    rows = np.arange(N)
+    assert np.array_equal(decoded(spec, rows, hm=0), MI.causal_document([120, 80], rows))
+    assert np.array_equal(decoded(spec, rows, hm=1), MI.causal(N, rows))
