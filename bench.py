@@ -45,8 +45,11 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # profiles/fwd_kernel_document_b1h8n32768d128.md) and scaled by 4 to H = 32:
 # every head is an independent unit of identical work, so traffic grows in
 # proportion to the heads.
-# Heads per chunk of the host-buffer pipeline the end-to-end leg times.
-E2E_CHUNK_HEADS = 4
+# Heads per chunk of the host-buffer pipeline the end-to-end leg times (on the
+# 32K document workload, chunks of 1, 2, 4, 8, 16 heads took 9.65, 7.48, 7.76,
+# 8.70, 10.71 ms per step on GB300: copy-bound, with the first copy-in and last
+# copy-out exposed).
+E2E_CHUNK_HEADS = 2
 
 NCU_TRAFFIC = {
     "bwd_main@e03f310508ff@document_b1h32n32768d128": 4 * (405.983488e6 + 220.970240e6),
