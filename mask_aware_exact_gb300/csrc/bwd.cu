@@ -267,11 +267,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_st = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t id_kd = idesc_bf16(128, D, 0, 1);    // dV, dK
       constexpr uint32_t id_dq = idesc_bf16(128, D, 1, 1);    // dQ (M = queries)
+      // Shared-memory descriptors are built once: every operand address here
+      // keeps the descriptor's 14-bit address field (16-byte units) below
+      // 2^14, so the descriptor of base + off is the base's plus off / 16.
+      const uint64_t kK = sdesc_sw128(sK, 16, 1024), kV = sdesc_sw128(sV, 16, 1024);
+      const uint64_t kQ = sdesc_sw128(sQ, 16, 1024), kDO = sdesc_sw128(sDO, 16, 1024);
+      const uint64_t kDS = sdesc_sw128(sDS, 16, 1024);
+      const uint64_t mDO = sdesc_sw128(sDO, 16384, 1024), mQ = sdesc_sw128(sQ, 16384, 1024);
+      const uint64_t mDS = sdesc_sw128(sDS, 16384, 1024), mK = sdesc_sw128(sK, 16384, 1024);
+      auto d16 = [](uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); };
       bool ok = mbar_wait(bar.kv_full(), 0, p.status);
       if (!ok) record_failure(p.status, kStatusTimeout, kSiteBwdKV);
       for (int t = 0; ok && t < ntiles; ++t) {
         const int st = t & 1;
-        const uint32_t q = sQ + st * L::kTileBytes, g = sDO + st * L::kTileBytes;
+        const uint64_t stage = d16(st * L::kTileBytes);
         if (!mbar_wait(bar.q_full(st), (t >> 1) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteBwdQ);
           break;
@@ -283,9 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q + off, 16, 1024),
-                 id_st, k > 0);
+          const uint64_t off = d16((k >> 2) * 16384 + (k & 3) * 32);
+          mma_ss(tmem + kColS, kK + off, kQ + stage + off, id_st, k > 0);
         }
         mma_commit(bar.s_full());
         if (t >= 1 && !mbar_wait(bar.dq_drained(), (t - 1) & 1, p.status)) {  // dQ_{t-1} read out
@@ -295,9 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(g + off, 16, 1024),
-                 id_st, k > 0);
+          const uint64_t off = d16((k >> 2) * 16384 + (k & 3) * 32);
+          mma_ss(tmem + kColDP, kV + off, kDO + stage + off, id_st, k > 0);
         }
         mma_commit(bar.dp_full());
         if (!mbar_wait(bar.pt_ready(), t & 1, p.status)) {
@@ -307,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + kColDV, tmem + pt_col(k), sdesc_sw128(g + k * 2048, 16384, 1024),
-                 id_kd, (t > 0 || k > 0));
+          mma_ts(tmem + kColDV, tmem + pt_col(k), mDO + stage + d16(k * 2048), id_kd,
+                 (t > 0 || k > 0));
         mma_commit(bar.dv_done());
         if (!mbar_wait(bar.ds_ready(), t & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteBwdDS);
@@ -317,15 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tmem + kColDK, sdesc_sw128(sDS + off, 16, 1024),
-                 sdesc_sw128(q + k * 2048, 16384, 1024), id_kd, (t > 0 || k > 0));
+          const uint64_t off = d16((k >> 2) * 16384 + (k & 3) * 32);
+          mma_ss(tmem + kColDK, kDS + off, mQ + stage + d16(k * 2048), id_kd, (t > 0 || k > 0));
         }
         // dQ_t = dS K: A = dS^T read MN-major (M = queries), B = K read MN-major
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + kColDP, sdesc_sw128(sDS + k * 2048, 16384, 1024),
-                 sdesc_sw128(sK + k * 2048, 16384, 1024), id_dq, k > 0);
+          mma_ss(tmem + kColDP, mDS + d16(k * 2048), mK + d16(k * 2048), id_dq, k > 0);
         mma_commit(bar.tile_done());
       }
     }

@@ -248,6 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
+      // Shared-memory descriptors are built once: the address field (bits
+      // 0-13, in 16-byte units) of every operand stays below 2^14 here, so a
+      // descriptor for base + off is the base descriptor plus off / 16. This
+      // keeps the per-MMA instruction stream of this thread short.
+      const uint64_t dq_base = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dk_base = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dv_base = sdesc_sw128(sV, 16384, 1024);
       // S_j; for j < 2 after waiting for K_j here, later ones after go(j - 2)
       auto issue_s = [&](int j) -> bool {
         const int slot = j % kKSlots, g = j % kSRegions;
@@ -258,12 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
         }
-        const uint32_t kb = sK + slot * L::kTileBytes;
+        const uint64_t kd = dk_base + static_cast<uint64_t>((slot * L::kTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * L::kChunk + (k & 3) * 32;
-          mma_ss(tmem + 128 * g, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                 idesc_s, k > 0);
+          const uint64_t off16 = static_cast<uint64_t>(((k >> 2) * L::kChunk + (k & 3) * 32) >> 4);
+          mma_ss(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, k > 0);
         }
         mma_commit(bar.s_full(g));  // also frees K slot j % 3
         return true;
@@ -279,10 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t vb = sV + vs * L::kTileBytes;
+        const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + kColO, tmem + 128 * g + 8 * k, sdesc_sw128(vb + k * 2048, 16384, 1024),
+          mma_ts(tmem + kColO, tmem + 128 * g + 8 * k, vd + static_cast<uint64_t>((k * 2048) >> 4),
                  idesc_pv, (j > 0 || k > 0));
         mma_commit(bar.pv_done(g));  // also frees V slot j % 3
         if (j + 2 < ntiles) issue_s(j + 2);  // its region and K slot are cleared by go(j)
