@@ -226,6 +226,19 @@ fm_status flashmask_localize(const fm_mask* mask, int B, int N, int row0, int ro
                              int32_t* lte, int32_t* uts, int32_t* ute, int32_t* inexact,
                              void* stream);
 
+/* Self-test of the failure path (no counterpart in the pages). Launches `ctas`
+ * (1..1024) one-warp CTAs whose mbarrier wait can never complete, bounded the
+ * way every wait of the library is: CTA 0 gives up after `limit_ns` (1e6..2e9)
+ * of wall time and records site 301 in the workspace status word; the other
+ * CTAs use the library's own limit but leave as soon as they see that status,
+ * as the CTAs of an attention kernel do when one of their waits fails. No
+ * fault, no hang; the context stays usable. Returns FM_OK once queued on
+ * `stream`; flashmask_check_status() then returns FM_ERR_TIMEOUT with detail
+ * 301. ws: any workspace of >= 16 bytes, 256-byte aligned (only the status
+ * word is used). */
+fm_status flashmask_selftest_timeout(void* ws, size_t ws_bytes, long long limit_ns, int ctas,
+                                     void* stream);
+
 /* Synchronises `stream`, then reads and clears the workspace status word.
  * Returns FM_ERR_TIMEOUT if a kernel wait gave up since the last check,
  * FM_ERR_CUDA if the stream reports an error, FM_OK otherwise. If detail is

@@ -18,6 +18,7 @@ enum Site : int {
   kSiteFwdVEmpty, kSiteFwdSmemAlign,
   kSiteBwdKV = 201, kSiteBwdQ, kSiteBwdQEmpty, kSiteBwdS, kSiteBwdDP, kSiteBwdPT, kSiteBwdDS,
   kSiteBwdDV, kSiteBwdDQ, kSiteBwdDrained, kSiteBwdDone, kSiteBwdSmemAlign,
+  kSiteSelftest = 301,
 };
 
 struct MaskDev {

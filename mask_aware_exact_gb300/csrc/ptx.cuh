@@ -65,11 +65,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete. Returns false if the
-// wall-time limit ran out first, or as soon as `abort_word` (the device status
-// word; may be null) is nonzero because some other wait of the grid gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          const int32_t* abort_word) {
+// Waits for the phase with the given parity to complete. Returns false if
+// `limit_ns` of wall time ran out first, or as soon as `abort_word` (the device
+// status word; may be null) is nonzero because some other wait of the grid gave up.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity,
+                                              const int32_t* abort_word, uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;  // already complete: no suspend
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -77,8 +77,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     if (abort_word != nullptr && *reinterpret_cast<const volatile int32_t*>(abort_word) != 0)
       return false;
-    if (global_timer_ns() - t0 > FM_WAIT_LIMIT_NS) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+// The wait every kernel of the library uses: limit FM_WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const int32_t* abort_word) {
+  return mbar_wait_for(bar, parity, abort_word, FM_WAIT_LIMIT_NS);
 }
 
 // ---------------------------------------------------------------- fences

@@ -39,8 +39,8 @@ class FmWsLayout(ctypes.Structure):
 EXPORTED = ("flashmask_workspace_bytes", "flashmask_workspace_layout", "flashmask_classify",
             "flashmask_fwd", "flashmask_bwd", "flashmask_bwd_preprocess", "flashmask_bwd_main",
             "flashmask_bwd_finalize", "flashmask_fwd_noalloc", "flashmask_host_workspace_bytes",
-            "flashmask_fwd_bwd_host", "flashmask_localize", "flashmask_check_status",
-            "flashmask_status_string")
+            "flashmask_fwd_bwd_host", "flashmask_localize", "flashmask_selftest_timeout",
+            "flashmask_check_status", "flashmask_status_string")
 
 _lib = None
 
@@ -83,6 +83,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.flashmask_fwd_bwd_host.restype = i
     L.flashmask_localize.argtypes = [ctypes.POINTER(_FmMask), i, i, i, i, vp, vp, vp, vp, vp, vp]
     L.flashmask_localize.restype = i
+    L.flashmask_selftest_timeout.argtypes = [vp, sz, ctypes.c_longlong, i, vp]
+    L.flashmask_selftest_timeout.restype = i
     L.flashmask_check_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
     L.flashmask_check_status.restype = i
     L.flashmask_status_string.argtypes = [i]
@@ -370,3 +372,9 @@ def flashmask_localize(mask: DeviceMask, B: int, N: int, row0: int, rows: int, s
                                      out[1].data_ptr(), out[2].data_ptr(), out[3].data_ptr(),
                                      flag.data_ptr(), _stream_ptr(stream)), "flashmask_localize")
     return DeviceMask(out[0], out[1], out[2], out[3], False), bool(flag.item())
+
+
+def flashmask_selftest_timeout(ws: torch.Tensor, limit_ns: int, ctas: int = 1, stream=None):
+    """Queues the bounded-wait self-test (see include/flashmask.h)."""
+    _check(load().flashmask_selftest_timeout(ws.data_ptr(), ws.numel(), int(limit_ns), int(ctas),
+                                             _stream_ptr(stream)), "flashmask_selftest_timeout")

@@ -111,3 +111,11 @@ def test_bwd_and_classify_argument_errors(lib):
     assert lib.flashmask_classify(ctypes.byref(m), 1, 256, FAKE, 8, None) == fm.FM_ERR_WORKSPACE
     assert lib.flashmask_workspace_layout(1, 2, 1, 256, 64, 1, None) == fm.FM_ERR_INVALID_ARG
     assert lib.flashmask_check_status(None, None, None) == fm.FM_ERR_WORKSPACE
+
+
+def test_selftest_argument_errors(lib):
+    assert lib.flashmask_selftest_timeout(None, 256, 10_000_000, 1, None) == fm.FM_ERR_WORKSPACE
+    assert lib.flashmask_selftest_timeout(FAKE, 8, 10_000_000, 1, None) == fm.FM_ERR_WORKSPACE
+    assert lib.flashmask_selftest_timeout(FAKE, 256, 10, 1, None) == fm.FM_ERR_INVALID_ARG
+    assert lib.flashmask_selftest_timeout(FAKE, 256, 10_000_000, 0, None) == fm.FM_ERR_INVALID_ARG
+    assert lib.flashmask_selftest_timeout(FAKE, 256, 3_000_000_000, 1, None) == fm.FM_ERR_INVALID_ARG
