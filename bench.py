@@ -52,8 +52,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 E2E_CHUNK_HEADS = 2
 
 NCU_TRAFFIC = {
-    "bwd_main@e03f310508ff@document_b1h32n32768d128": 4 * (405.983488e6 + 220.970240e6),
-    "fwd@16dc441880ce@document_b1h32n32768d128": 4 * (201.948672e6 + 49.610752e6),
+    "bwd_main@0a6057c01ca0@document_b1h32n32768d128": 4 * (405.966336e6 + 220.942848e6),
+    "fwd@c5f69ef45d2f@document_b1h32n32768d128": 4 * (201.917440e6 + 49.920768e6),
 }
 
 
