@@ -379,15 +379,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             mb[hh] = column_mask_bits(key, lts, lte, uts, ute, causal,
                                       qb * kTile + 64 * g + 32 * hh);
         }
+        const uint64_t c2 = f2_make(c, c);
 #pragma unroll
         for (int i4 = 0; i4 < 16; ++i4) {
           const float4 l4 = reinterpret_cast<const float4*>(ls)[i4];  // broadcast
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const uint64_t nl2[2] = {f2_make(-l4.x, -l4.y), f2_make(-l4.z, -l4.w)};
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int q0 = 4 * i4 + 2 * u;
-            float p0 = ex2(fmaf(__uint_as_float(v[q0]), c, -lv[2 * u]));
-            float p1 = ex2(fmaf(__uint_as_float(v[q0 + 1]), c, -lv[2 * u + 1]));
+            // s * c - lse2 for a pair of queries in one paired fp32 instruction
+            float x0, x1;
+            f2_split(f2_fma(f2_make(__uint_as_float(v[q0]), __uint_as_float(v[q0 + 1])), c2,
+                            nl2[u]),
+                     x0, x1);
+            float p0 = ex2(x0), p1 = ex2(x1);
             p0 = ((mb[q0 >> 5] >> (q0 & 31)) & 1u) ? 0.f : p0;
             p1 = ((mb[q0 >> 5] >> ((q0 + 1) & 31)) & 1u) ? 0.f : p1;
             pk[2 * i4 + u] = pack_bf16x2(p0, p1);
@@ -422,14 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
           const float4 d4 = reinterpret_cast<const float4*>(dl + 32 * hh)[i4];  // broadcast
-          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          const uint64_t nd2[2] = {f2_make(-d4.x, -d4.y), f2_make(-d4.z, -d4.w)};
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int i = 2 * i4 + u;
             const uint32_t pw = pk[16 * hh + i];
-            const float d0 = __uint_as_float(pw << 16) * (__uint_as_float(v[2 * i]) - dv4[2 * u]);
-            const float d1 = __uint_as_float(pw & 0xffff0000u) *
-                             (__uint_as_float(v[2 * i + 1]) - dv4[2 * u + 1]);
+            // P (dP - D) for a pair of queries in two paired fp32 instructions
+            const uint64_t dd = f2_add(f2_make(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                       nd2[u]);
+            float d0, d1;
+            f2_split(f2_mul(f2_make(__uint_as_float(pw << 16), __uint_as_float(pw & 0xffff0000u)), dd),
+                     d0, d1);
             dk[i] = pack_bf16x2(d0, d1);
           }
         }

@@ -394,16 +394,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = m_new;
         }
         const float m_use = (m == -INFINITY) ? 0.f : m;
-        float l0 = 0.f, l1 = 0.f;
+        // pairs of columns through the paired fp32 instructions: s * c - m
+        // and the running pair of partial sums take one issue slot per pair
+        const uint64_t c2 = f2_make(c, c), nm2 = f2_make(-m_use, -m_use);
+        uint64_t l2 = f2_make(0.f, 0.f);
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), c, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), c, -m_use));
-          l0 += p0;
-          l1 += p1;
+          float x0, x1;
+          f2_split(f2_fma(f2_make(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), c2,
+                          nm2),
+                   x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          l2 = f2_add(l2, f2_make(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
+        float l0, l1;
+        f2_split(l2, l0, l1);
         l = l * alpha + (l0 + l1);
         // P_j over this warpgroup's part of S_j's region: keys [64w, 64w+64)
         // as bf16 pairs in columns [32w, 32w+32) (the A operand of P V)
