@@ -52,8 +52,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 E2E_CHUNK_HEADS = 2
 
 NCU_TRAFFIC = {
-    "bwd_main@0a6057c01ca0@document_b1h32n32768d128": 4 * (405.966336e6 + 220.942848e6),
-    "fwd@c5f69ef45d2f@document_b1h32n32768d128": 4 * (201.917440e6 + 49.920768e6),
+    "bwd_main@3a87d70f205c@document_b1h32n32768d128": 4 * (405.988096e6 + 220.376832e6),
+    "fwd@876944492112@document_b1h32n32768d128": 4 * (201.910016e6 + 50.058752e6),
 }
 
 
