@@ -78,16 +78,6 @@ struct BwdBars {
   __device__ uint32_t dq_drained() const { return base + 8 * 11; }
 };
 
-__device__ __forceinline__ void record_failure(int32_t* status, int bit, int site) {
-  atomicOr(&status[0], bit);
-  atomicCAS(&status[1], 0, site);
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {

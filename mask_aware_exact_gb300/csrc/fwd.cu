@@ -85,16 +85,6 @@ struct FwdBars {
   }
 };
 
-__device__ __forceinline__ void record_failure(int32_t* status, int bit, int site) {
-  atomicOr(&status[0], bit);
-  atomicCAS(&status[1], 0, site);
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // The 256 softmax threads (both warpgroups).
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }

@@ -24,10 +24,7 @@ __global__ void __launch_bounds__(32) selftest_timeout_kernel(int32_t* status, u
   if (threadIdx.x != 0) return;
   const bool ok = blockIdx.x == 0 ? mbar_wait_for(b, 0, status, short_ns)
                                   : mbar_wait(b, 0, status);
-  if (!ok) {
-    atomicOr(&status[0], kStatusTimeout);
-    atomicCAS(&status[1], 0, kSiteSelftest);
-  }
+  if (!ok) record_failure(status, kStatusTimeout, kSiteSelftest);
 }
 
 }  // namespace
