@@ -177,6 +177,44 @@ fm_status flashmask_fwd_noalloc(const void* q, const void* k, const void* v, con
                                 int B, int H, int N, int d, float scale, void* o, float* lse,
                                 void* stream);
 
+/* FP8 forward ("FlashAttention-3", abstract: block quantization for FP8
+ * attention): the same inputs, mask and outputs as flashmask_fwd (bf16 Q, K, V
+ * [B,H,N,d], bf16 O and fp32 LSE), with the two products of each tile taken in
+ * e4m3 on the tensor cores. d must be 128 (FM_ERR_UNSUPPORTED otherwise).
+ * Each call quantises into the workspace: Q and K with one scale per head and
+ * 128-row block (scale = absmax / 448, values rounded to nearest even and
+ * saturated), V transposed with one scale per head; P is rounded to e4m3 as
+ * 28 * P before P V (the running maximum is allowed to lag the true one by
+ * at most 4 in log2 units, so 28 * P <= 448). The row sums, the running
+ * maximum, LSE and every
+ * accumulation stay fp32, so LSE carries only the error of the quantised
+ * scores. Results differ from flashmask_fwd by the e4m3 rounding (3 mantissa
+ * bits, relative step 2^-4): on random data O's relative Frobenius error is a
+ * few percent, not the bf16 path's 1e-3.
+ *   Workspace: flashmask_fwd_fp8_workspace_bytes(B, H, Hm, N) bytes, 256-byte
+ *   aligned; its first part is the forward workspace layout (for_bwd = 0) of
+ *   flashmask_workspace_layout with d = 128, so ws_classified works as in
+ *   flashmask_fwd and flashmask_check_status reads its status word. The rest,
+ *   at the byte offsets flashmask_fwd_fp8_layout gives, holds what the call
+ *   wrote last (the caller may read it back):
+ *     q8, k8   e4m3   [B,H,N,128]     Q / scale_Q, K / scale_K
+ *     vt8      e4m3   [B,H,128,Npad]  (V / scale_V)^T, keys >= N zero
+ *     qscale   fp32   [B,H,Tr]        scale_Q of each 128-row block
+ *     kscale   fp32   [B,H,Tr]        scale_K of each 128-row block
+ *     vscale   fp32   [B,H]           scale_V of each head
+ *   A scale is absmax / 448 computed in fp32 (1 for an all-zero block) and a
+ *   value is e4m3(x * (1 / scale)), both products rounded in fp32. The size
+ *   function returns 0, the layout function FM_ERR_UNSUPPORTED, for an
+ *   unsupported shape. Asynchronous on `stream`. */
+typedef struct {
+  size_t fwd_total, q8, k8, vt8, qscale, kscale, vscale, total;
+} fm_fp8_layout;
+size_t flashmask_fwd_fp8_workspace_bytes(int B, int H, int Hm, int N);
+fm_status flashmask_fwd_fp8_layout(int B, int H, int Hm, int N, fm_fp8_layout* out);
+fm_status flashmask_fwd_fp8(const void* q, const void* k, const void* v, const fm_mask* mask,
+                            int B, int H, int N, int d, float scale, void* o, float* lse, void* ws,
+                            size_t ws_bytes, int ws_classified, void* stream);
+
 /* Forward and backward between HOST buffers, for callers whose tensors live in
  * host memory (the pages have no counterpart; the computation is exactly
  * flashmask_classify + flashmask_fwd + flashmask_bwd). The heads are cut into

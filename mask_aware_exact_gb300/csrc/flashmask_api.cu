@@ -149,6 +149,50 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, int d) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map over a [rows, cols] byte matrix (e4m3) with 128 x 128-byte boxes
+// and 128-byte swizzle.
+bool make_map_u8(CUtensorMap* m, const void* base, long long rows, long long cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Workspace of the FP8 forward: the forward's classification layout, then the
+// e4m3 operands and their scales.
+struct Fp8Layout {
+  fm_ws_layout base;
+  size_t q8, k8, vt8, qscale, kscale, vscale, vamax, total;
+};
+
+Fp8Layout make_fp8_layout(int B, int H, int Hm, int N) {
+  Fp8Layout F;
+  F.base = make_layout(B, H, Hm, N, 128, 0);
+  const size_t BH = static_cast<size_t>(B) * H, Tr = blocks_of(N);
+  size_t off = F.base.total;
+  F.q8 = off;
+  off = align_up(off + BH * N * 128, 256);
+  F.k8 = off;
+  off = align_up(off + BH * N * 128, 256);
+  F.vt8 = off;
+  off = align_up(off + BH * 128 * padded(N), 256);
+  F.qscale = off;
+  off = align_up(off + BH * Tr * 4, 256);
+  F.kscale = off;
+  off = align_up(off + BH * Tr * 4, 256);
+  F.vscale = off;
+  off = align_up(off + BH * 4, 256);
+  F.vamax = off;
+  off = align_up(off + BH * 4, 256);
+  F.total = off;
+  return F;
+}
+
 fm_status check_ws(void* ws, size_t ws_bytes, const fm_ws_layout& L) {
   if (!ws) return FM_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FM_ERR_WORKSPACE;
@@ -214,6 +258,7 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
   p.Tr = blocks_of(N);
   p.Tc = blocks_of(N);
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.qscale = p.kscale = p.vscale = nullptr;
   p.row_count = t.row_count;
   p.row_list = t.row_list;
   p.row_order = t.row_order;
@@ -221,6 +266,81 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
   p.lse = lse;
   p.status = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.status);
   return fm::launch_fwd(d, mq, mk, mv, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+size_t flashmask_fwd_fp8_workspace_bytes(int B, int H, int Hm, int N) {
+  if (!shape_ok(B, H, Hm, N, 128)) return 0;
+  return make_fp8_layout(B, H, Hm, N).total;
+}
+
+fm_status flashmask_fwd_fp8_layout(int B, int H, int Hm, int N, fm_fp8_layout* out) {
+  if (!out) return FM_ERR_INVALID_ARG;
+  if (!shape_ok(B, H, Hm, N, 128)) return FM_ERR_UNSUPPORTED;
+  const Fp8Layout F = make_fp8_layout(B, H, Hm, N);
+  out->fwd_total = F.base.total;
+  out->q8 = F.q8;
+  out->k8 = F.k8;
+  out->vt8 = F.vt8;
+  out->qscale = F.qscale;
+  out->kscale = F.kscale;
+  out->vscale = F.vscale;
+  out->total = F.total;
+  return FM_OK;
+}
+
+fm_status flashmask_fwd_fp8(const void* q, const void* k, const void* v, const fm_mask* mask,
+                            int B, int H, int N, int d, float scale, void* o, float* lse, void* ws,
+                            size_t ws_bytes, int ws_classified, void* stream) {
+  if (!q || !k || !v || !o || !lse || !mask_ok(mask)) return FM_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FM_ERR_INVALID_ARG;
+  if (d != 128 || !shape_ok(B, H, mask->Hm, N, d)) return FM_ERR_UNSUPPORTED;
+  const Fp8Layout F = make_fp8_layout(B, H, mask->Hm, N);
+  fm_ws_layout whole = F.base;
+  whole.total = F.total;
+  const fm_status ws_st = check_ws(ws, ws_bytes, whole);
+  if (ws_st != FM_OK) return ws_st;
+  char* w = static_cast<char*>(ws);
+  fm::Fp8Operands f;
+  f.q8 = reinterpret_cast<uint8_t*>(w + F.q8);
+  f.k8 = reinterpret_cast<uint8_t*>(w + F.k8);
+  f.vt8 = reinterpret_cast<uint8_t*>(w + F.vt8);
+  f.qscale = reinterpret_cast<float*>(w + F.qscale);
+  f.kscale = reinterpret_cast<float*>(w + F.kscale);
+  f.vscale = reinterpret_cast<float*>(w + F.vscale);
+  f.vamax = reinterpret_cast<unsigned int*>(w + F.vamax);
+  const int BH = B * H;
+  const long long rows = static_cast<long long>(BH) * N;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_u8(&mq, f.q8, rows, 128) || !make_map_u8(&mk, f.k8, rows, 128) ||
+      !make_map_u8(&mv, f.vt8, static_cast<long long>(BH) * 128, padded(N)))
+    return FM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const fm::ClassifyTables t = tables(F.base, ws);
+  if (!ws_classified) {
+    if (fm::launch_classify(mask_dev(mask), B, N, t, s) != cudaSuccess) return FM_ERR_CUDA;
+  }
+  if (fm::launch_quant_fp8(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
+                           static_cast<const uint16_t*>(v), BH, N, f, s) != cudaSuccess)
+    return FM_ERR_CUDA;
+  fm::FwdParams p;
+  p.mask = mask_dev(mask);
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.Tr = blocks_of(N);
+  p.Tc = blocks_of(N);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.qscale = f.qscale;
+  p.kscale = f.kscale;
+  p.vscale = f.vscale;
+  p.row_count = t.row_count;
+  p.row_list = t.row_list;
+  p.row_order = t.row_order;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.status = reinterpret_cast<int32_t*>(w + F.base.status);
+  return fm::launch_fwd_fp8(mq, mk, mv, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
 fm_status flashmask_bwd_preprocess(const void* o, const float* lse, const void* dout, int B, int H,

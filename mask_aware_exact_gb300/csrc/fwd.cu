@@ -37,6 +37,7 @@
 // has completed.
 #include "internal.h"
 #include "ptx.cuh"
+#include "ptx_fp8.cuh"
 #include "flashmask.h"
 
 namespace fm {
@@ -48,11 +49,16 @@ constexpr int kSRegions = 3;  // TMEM S/P regions of 128 columns
 constexpr int kKSlots = 3, kVSlots = 3;
 constexpr uint32_t kColO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// FP8: P is stored as e4m3(p * kFp8PScale). With the running maximum lagging
+// by at most kRescaleThresholdFp8 (log2 units), p < 2^threshold and
+// p * kFp8PScale stays below 448, the largest finite e4m3 value.
+constexpr float kRescaleThresholdFp8 = 4.0f;
+constexpr float kFp8PScale = 28.0f;
 
-template <int D>
+template <int D, bool kFp8>
 struct FwdLayout {
-  static constexpr int kTileBytes = kTile * D * 2;  // one 128 x d bf16 tile
-  static constexpr int kChunks = D / 64;            // 64-column (128-byte) TMA boxes
+  static constexpr int kTileBytes = kTile * D * (kFp8 ? 1 : 2);  // one 128 x d tile
+  static constexpr int kChunks = kFp8 ? 1 : D / 64;  // 128-byte-wide TMA boxes per tile
   static constexpr int kChunk = 16384;              // 128 rows x 128 bytes
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;             // kKSlots x kTileBytes
@@ -136,11 +142,15 @@ __device__ __forceinline__ void tmem_cols_to_bf16(uint32_t taddr, bool live, flo
   }
 }
 
-template <int D, bool kShortLast>  // kShortLast: N is not a multiple of 128
+// kShortLast: N is not a multiple of 128. kFp8 (d = 128 only): e4m3 Q, K and
+// transposed V with block scales, kind::f8f6f4 MMAs (K = 32 per instruction),
+// P stored as e4m3(p * 256).
+template <int D, bool kShortLast, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const FwdParams p) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, kFp8>;
+  static_assert(!kFp8 || D == 128, "the FP8 forward is for d = 128");
   constexpr int kOCols = D / 2;  // O columns per softmax warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -227,24 +237,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(bar.v_full(slot), L::kTileBytes);
-        const int vrow = head_row0 + (list[j] >> 2) * kTile;
-        for (int ch = 0; ch < L::kChunks; ++ch)
-          tma_load_2d(sV + slot * L::kTileBytes + ch * L::kChunk, &mv, ch * 64, vrow,
+        if constexpr (kFp8) {
+          // V^T tile: the head's 128 rows of d, the block's 128 keys
+          tma_load_2d(sV + slot * L::kTileBytes, &mv, (list[j] >> 2) * kTile, bh * 128,
                       bar.v_full(slot));
+        } else {
+          const int vrow = head_row0 + (list[j] >> 2) * kTile;
+          for (int ch = 0; ch < L::kChunks; ++ch)
+            tma_load_2d(sV + slot * L::kTileBytes + ch * L::kChunk, &mv, ch * 64, vrow,
+                        bar.v_full(slot));
+        }
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
+      constexpr uint32_t idesc_s = kFp8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, 0, 1);
+      constexpr int kSSteps = kFp8 ? D / 32 : D / 16;  // K steps of S = Q K^T
+      constexpr int kPvSteps = kFp8 ? 4 : 8;           // K steps (keys) of O += P V
       // Shared-memory descriptors are built once: the address field (bits
       // 0-13, in 16-byte units) of every operand stays below 2^14 here, so a
       // descriptor for base + off is the base descriptor plus off / 16. This
       // keeps the per-MMA instruction stream of this thread short.
       const uint64_t dq_base = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk_base = sdesc_sw128(sK, 16, 1024);
-      const uint64_t dv_base = sdesc_sw128(sV, 16384, 1024);
+      // V is MN-major [keys][d] in bf16, K-major [d][keys] as e4m3 V^T
+      const uint64_t dv_base = kFp8 ? sdesc_sw128(sV, 16, 1024) : sdesc_sw128(sV, 16384, 1024);
       // S_j; for j < 2 after waiting for K_j here, later ones after go(j - 2)
       auto issue_s = [&](int j) -> bool {
         const int slot = j % kKSlots, g = j % kSRegions;
@@ -257,9 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint64_t kd = dk_base + static_cast<uint64_t>((slot * L::kTileBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < kSSteps; ++k) {
+          // 32 bytes of each 128-byte row per K step (16 bf16 or 32 e4m3)
           const uint64_t off16 = static_cast<uint64_t>(((k >> 2) * L::kChunk + (k & 3) * 32) >> 4);
-          mma_ss(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, k > 0);
+          if constexpr (kFp8)
+            mma_ss_f8(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, k > 0);
+          else
+            mma_ss(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, k > 0);
         }
         mma_commit(bar.s_full(g));  // also frees K slot j % 3
         return true;
@@ -277,9 +300,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + kColO, tmem + 128 * g + 8 * k, vd + static_cast<uint64_t>((k * 2048) >> 4),
-                 idesc_pv, (j > 0 || k > 0));
+        for (int k = 0; k < kPvSteps; ++k) {
+          // A: P, 8 TMEM columns per K step; B: the next 16 key rows of V
+          // (bf16) or the next 32 key bytes of each row of V^T (e4m3)
+          if constexpr (kFp8)
+            mma_ts_f8(tmem + kColO, tmem + 128 * g + 8 * k,
+                      vd + static_cast<uint64_t>((k * 32) >> 4), idesc_pv, (j > 0 || k > 0));
+          else
+            mma_ts(tmem + kColO, tmem + 128 * g + 8 * k,
+                   vd + static_cast<uint64_t>((k * 2048) >> 4), idesc_pv, (j > 0 || k > 0));
+        }
         mma_commit(bar.pv_done(g));  // also frees V slot j % 3
         if (j + 2 < ntiles) issue_s(j + 2);  // its region and K slot are cleared by go(j)
       }
@@ -309,7 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w = warp >> 2;                 // warpgroup: key columns [64w, 64w+64)
     const int row = (warp & 3) * 32 + lane;  // query row within the block = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const float c = p.scale_log2;
+    // FP8: the true score is S times scale_Q(query block) * scale_K(key
+    // block); the product folds into each tile's exponent scale c
+    const float c_row = kFp8 ? p.scale_log2 * p.qscale[static_cast<size_t>(bh) * p.Tr + r]
+                             : p.scale_log2;
+    constexpr float kThresh = kFp8 ? kRescaleThresholdFp8 : kRescaleThreshold;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     int next_entry = ntiles > 0 ? list[0] : 0;  // read one step ahead
@@ -320,6 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int entry = next_entry;
       if (j + 1 < ntiles) next_entry = list[j + 1];
       const int g = j % kSRegions;
+      const float c =
+          kFp8 ? c_row * p.kscale[static_cast<size_t>(bh) * p.Tc + (entry >> 2)] : c_row;
       // The element mask applies on PARTIAL tiles and on every tile of a short
       // last key block (its keys >= N do not exist and are masked).
       const bool short_keys = kShortLast && (entry >> 2) == p.Tc - 1;
@@ -377,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         const float mx = fmaxf(pm, red[((j & 1) * 2 + (w ^ 1)) * kTile + row]);
         const float m_new = fmaxf(m, mx);
-        const bool rescale = m_new > m + kRescaleThreshold;
+        const bool rescale = m_new > m + kThresh;
         float alpha = 1.f;
         if (rescale) {
           alpha = ex2(m - m_new);
@@ -388,7 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // and the running pair of partial sums take one issue slot per pair
         const uint64_t c2 = f2_make(c, c), nm2 = f2_make(-m_use, -m_use);
         uint64_t l2 = f2_make(0.f, 0.f);
-        uint32_t pk[32];
+        uint32_t pk[32];  // bf16 pairs; FP8: e4m3 quads in pk[0..15]
+        float pq0 = 0.f, pq1 = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           float x0, x1;
@@ -397,14 +434,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                    x0, x1);
           const float p0 = ex2(x0), p1 = ex2(x1);
           l2 = f2_add(l2, f2_make(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+          if constexpr (kFp8) {
+            // the scale keeps small probabilities above e4m3's subnormal range
+            if (i & 1)
+              pk[i >> 1] = pack_e4m3x4(pq0, pq1, p0 * kFp8PScale, p1 * kFp8PScale);
+            else
+              pq0 = p0 * kFp8PScale, pq1 = p1 * kFp8PScale;
+          } else {
+            pk[i] = pack_bf16x2(p0, p1);
+          }
         }
         float l0, l1;
         f2_split(l2, l0, l1);
         l = l * alpha + (l0 + l1);
         // P_j over this warpgroup's part of S_j's region: keys [64w, 64w+64)
         // as bf16 pairs in columns [32w, 32w+32) (the A operand of P V)
-        tmem_st32p(tmem + lane_base + 128 * g + 32 * w, pk);
+        if constexpr (kFp8) {
+          // ... or as e4m3 quads in columns [16w, 16w+16)
+          tmem_st16(tmem + lane_base + 128 * g + 16 * w,
+                    *reinterpret_cast<const uint32_t(*)[16]>(pk));
+        } else {
+          tmem_st32p(tmem + lane_base + 128 * g + 32 * w, pk);
+        }
         if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
           // O is rescaled once O += P_{j-1} V_{j-1} has completed
           ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done((j - 1) % kSRegions),
@@ -440,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float ltot = l + lsum[(w ^ 1) * kTile + row];
     const bool live = ok && ntiles > 0;
     const bool has = live && ltot > 0.f;
-    const float inv = has ? 1.f / ltot : 0.f;
+    // FP8: O accumulated (kFp8PScale P) (V / scale_V)
+    const float inv = has ? (kFp8 ? p.vscale[bh] * (1.f / kFp8PScale) : 1.f) / ltot : 0.f;
     // rows >= N of a short last query block do not exist: nothing is stored
     const bool row_exists = !kShortLast || r * kTile + row < p.N;
     uint16_t* orow = p.o + static_cast<size_t>(q_row0 + row) * D + w * kOCols;
@@ -462,15 +514,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kShortLast>
+template <int D, bool kShortLast, bool kFp8 = false>
 cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const FwdParams& p, cudaStream_t s) {
-  using L = FwdLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kShortLast>,
+  using L = FwdLayout<D, kFp8>;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kShortLast, kFp8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.B * p.H * p.Tr);
-  fwd_kernel<D, kShortLast><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, p);
+  fwd_kernel<D, kShortLast, kFp8><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -484,6 +536,12 @@ cudaError_t launch_fwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, cons
                       : launch_fwd_t<64, false>(mq, mk, mv, p, s);
   return short_last ? launch_fwd_t<128, true>(mq, mk, mv, p, s)
                     : launch_fwd_t<128, false>(mq, mk, mv, p, s);
+}
+
+cudaError_t launch_fwd_fp8(const CUtensorMap& mq8, const CUtensorMap& mk8,
+                           const CUtensorMap& mvt8, const FwdParams& p, cudaStream_t s) {
+  return p.N % kTile != 0 ? launch_fwd_t<128, true, true>(mq8, mk8, mvt8, p, s)
+                          : launch_fwd_t<128, false, true>(mq8, mk8, mvt8, p, s);
 }
 
 }  // namespace fm

@@ -42,10 +42,26 @@ struct ClassifyTables {
   int32_t* col_order;  // [B,Hm,Tc]
 };
 
+// FP8 operands of the FP8 forward (in the workspace): Q and K e4m3 [B*H, N, 128]
+// with one scale per (head, 128-row block); V transposed, e4m3 [B*H, 128, Npad],
+// with one scale per head.
+struct Fp8Operands {
+  uint8_t* q8;
+  uint8_t* k8;
+  uint8_t* vt8;
+  float* qscale;        // [B*H, Tr]
+  float* kscale;        // [B*H, Tr]
+  float* vscale;        // [B*H]
+  unsigned int* vamax;  // [B*H] scratch
+};
+
 struct FwdParams {
   MaskDev mask;
   int B, H, N, Tr, Tc;
   float scale_log2;  // scale * log2(e)
+  const float* qscale;  // FP8 forward only: per-block scales of Q, K and per-head scale of V
+  const float* kscale;
+  const float* vscale;
   const int32_t* row_count;
   const int32_t* row_list;
   const int32_t* row_order;
@@ -75,6 +91,10 @@ cudaError_t launch_classify(const MaskDev& m, int B, int N, const ClassifyTables
                             cudaStream_t s);
 cudaError_t launch_fwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const FwdParams& p, cudaStream_t s);
+cudaError_t launch_fwd_fp8(const CUtensorMap& mq8, const CUtensorMap& mk8,
+                           const CUtensorMap& mvt8, const FwdParams& p, cudaStream_t s);
+cudaError_t launch_quant_fp8(const uint16_t* q, const uint16_t* k, const uint16_t* v, int BH,
+                             int N, const Fp8Operands& f, cudaStream_t s);
 cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
                            float* delta, float* lse2, float* dq_accum, long long heads, int N,
                            int Npad, cudaStream_t s);

@@ -36,10 +36,16 @@ class FmWsLayout(ctypes.Structure):
                  "col_count", "col_list", "col_order", "lse2", "delta", "dq_accum", "total")]
 
 
+class FmFp8Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("fwd_total", "q8", "k8", "vt8", "qscale", "kscale", "vscale", "total")]
+
+
 EXPORTED = ("flashmask_workspace_bytes", "flashmask_workspace_layout", "flashmask_classify",
             "flashmask_fwd", "flashmask_bwd", "flashmask_bwd_preprocess", "flashmask_bwd_main",
             "flashmask_bwd_finalize", "flashmask_fwd_noalloc", "flashmask_host_workspace_bytes",
             "flashmask_fwd_bwd_host", "flashmask_localize", "flashmask_selftest_timeout",
+            "flashmask_fwd_fp8_workspace_bytes", "flashmask_fwd_fp8_layout", "flashmask_fwd_fp8",
             "flashmask_check_status", "flashmask_status_string")
 
 _lib = None
@@ -76,6 +82,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.flashmask_fwd_noalloc.argtypes = [vp, vp, vp, ctypes.POINTER(_FmMask), i, i, i, i, f, vp, vp,
                                         vp]
     L.flashmask_fwd_noalloc.restype = i
+    L.flashmask_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
+    L.flashmask_fwd_fp8_workspace_bytes.restype = sz
+    L.flashmask_fwd_fp8_layout.argtypes = [i, i, i, i, ctypes.POINTER(FmFp8Layout)]
+    L.flashmask_fwd_fp8_layout.restype = i
+    L.flashmask_fwd_fp8.argtypes = [vp, vp, vp, ctypes.POINTER(_FmMask), i, i, i, i, f, vp, vp, vp,
+                                    sz, i, vp]
+    L.flashmask_fwd_fp8.restype = i
     L.flashmask_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
     L.flashmask_host_workspace_bytes.restype = sz
     L.flashmask_fwd_bwd_host.argtypes = [vp, vp, vp, vp, ctypes.POINTER(_FmMask), i, i, i, i, f, vp,
@@ -182,6 +195,63 @@ def flashmask_fwd(q, k, v, mask: DeviceMask, ws, scale=None, o=None, lse=None, w
     _check(load().flashmask_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(m), B, H, N,
                                 d, scale, o.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(),
                                 int(bool(ws_classified)), _stream_ptr(stream)), "flashmask_fwd")
+    return o, lse
+
+
+def flashmask_fwd_fp8_workspace_bytes(B, H, Hm, N) -> int:
+    return load().flashmask_fwd_fp8_workspace_bytes(B, H, Hm, N)
+
+
+def flashmask_fwd_fp8_layout(B, H, Hm, N) -> FmFp8Layout:
+    out = FmFp8Layout()
+    _check(load().flashmask_fwd_fp8_layout(B, H, Hm, N, ctypes.byref(out)),
+           "flashmask_fwd_fp8_layout")
+    return out
+
+
+def read_fp8_operands(ws, B, H, Hm, N):
+    """The e4m3 operands and scales the last FP8 forward left in `ws`, as torch
+    tensors on its device: q8, k8 uint8 [B,H,N,128], vt8 uint8 [B,H,128,Npad],
+    qscale, kscale fp32 [B,H,Tr], vscale fp32 [B,H]."""
+    L = flashmask_fwd_fp8_layout(B, H, Hm, N)
+    Tr = (N + 127) // 128
+    Npad = 128 * Tr
+
+    def part(off, n):
+        return ws[off:off + n]
+    q8 = part(L.q8, B * H * N * 128).view(B, H, N, 128)
+    k8 = part(L.k8, B * H * N * 128).view(B, H, N, 128)
+    vt8 = part(L.vt8, B * H * 128 * Npad).view(B, H, 128, Npad)
+    qs = part(L.qscale, B * H * Tr * 4).view(torch.float32).view(B, H, Tr)
+    ks = part(L.kscale, B * H * Tr * 4).view(torch.float32).view(B, H, Tr)
+    vs = part(L.vscale, B * H * 4).view(torch.float32).view(B, H)
+    return q8, k8, vt8, qs, ks, vs
+
+
+def alloc_fp8_workspace(B, H, Hm, N, device="cuda") -> torch.Tensor:
+    n = flashmask_fwd_fp8_workspace_bytes(B, H, Hm, N)
+    if n == 0:
+        raise FlashMaskError(FM_ERR_UNSUPPORTED, "flashmask_fwd_fp8_workspace_bytes")
+    ws = torch.zeros(n, dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def flashmask_fwd_fp8(q, k, v, mask: DeviceMask, ws, scale=None, o=None, lse=None,
+                      ws_classified=False, stream=None):
+    """FP8 (e4m3) forward of bf16 Q, K, V with d = 128; returns (O bf16, LSE fp32)
+    like flashmask_fwd. `ws` comes from alloc_fp8_workspace."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _bf16(t, n)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    m = mask.c_struct()
+    _check(load().flashmask_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), ctypes.byref(m), B, H,
+                                    N, d, scale, o.data_ptr(), lse.data_ptr(), ws.data_ptr(),
+                                    ws.numel(), int(bool(ws_classified)), _stream_ptr(stream)),
+           "flashmask_fwd_fp8")
     return o, lse
 
 
