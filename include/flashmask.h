@@ -85,7 +85,8 @@ typedef struct {
 /* Byte offsets of the workspace regions (from the workspace base), for callers
  * that want to read the classification. Regions marked [bwd] exist only when
  * the workspace was sized with for_bwd != 0 (otherwise their offsets are 0).
- *   status    int32[4]                   device status word (0 = OK) + detail
+ *   status    int32[4]                   device status word (0 = OK), detail, and the
+ *                                        forward's work-item counter (reset by each call)
  *   minmax    int32  [B,Hm,Tc,8]         per key block: min/max of LTS, LTE, UTS, UTE
  *   labels    uint8  [B,Hm,Tr,Tc]        tile label, query-block major
  *   labels_t  uint8  [B,Hm,Tc,Tr]        tile label, key-block major

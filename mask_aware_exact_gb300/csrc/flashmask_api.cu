@@ -100,6 +100,21 @@ fm::MaskDev mask_dev(const fm_mask* m) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SMs of the current device (the persistent forward's grid), looked up once
+// per device.
+int sm_count() {
+  constexpr int kMaxDev = 256;
+  static int cached[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;  // a race between threads writes the same value
+  }
+  return cached[dev];
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // dependency on libcuda).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -265,6 +280,9 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.status = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.status);
+  p.sched = p.status + 2;  // third word of the 16-byte status region
+  p.num_sms = sm_count();
+  if (p.num_sms <= 0) return FM_ERR_CUDA;
   return fm::launch_fwd(d, mq, mk, mv, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
@@ -340,6 +358,9 @@ fm_status flashmask_fwd_fp8(const void* q, const void* k, const void* v, const f
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.status = reinterpret_cast<int32_t*>(w + F.base.status);
+  p.sched = p.status + 2;
+  p.num_sms = sm_count();
+  if (p.num_sms <= 0) return FM_ERR_CUDA;
   return fm::launch_fwd_fp8(mq, mk, mv, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 

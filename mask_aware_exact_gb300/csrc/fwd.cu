@@ -65,12 +65,14 @@ struct FwdLayout {
   static constexpr int kV = kK + kKSlots * kTileBytes;   // kVSlots x kTileBytes
   static constexpr int kRed = kV + kVSlots * kTileBytes;  // fp32 [2 parity][2 groups][128]
   static constexpr int kBar = kRed + 2 * 2 * kTile * 4;
-  // q_full, k_full[3], v_full[3], s_full[3], p_full[3], pv_done[3], go[3]. K slot,
-  // V slot and S region of block j are all j % 3, so "S_j done" also frees
-  // K slot j % 3 and "P_j V_j done" also frees V slot j % 3.
+  // q_full, k_full[3], v_full[3], s_full[3], p_full[3], pv_done[3], go[3],
+  // sched_full[2], sched_empty[2], o_free. K slot, V slot and S region of step
+  // J are all J % 3, so "S_J done" also frees K slot J % 3 and "P_J V_J done"
+  // also frees V slot J % 3.
   static_assert(kKSlots == kSRegions && kVSlots == kSRegions, "slots follow the S regions");
-  static constexpr int kNumBars = 1 + kKSlots + kVSlots + 4 * kSRegions;
-  static constexpr int kTmemSlot = kBar + kNumBars * 8;
+  static constexpr int kNumBars = 1 + kKSlots + kVSlots + 4 * kSRegions + 5;
+  static constexpr int kSched = kBar + kNumBars * 8;  // int[4]
+  static constexpr int kTmemSlot = kSched + 16;
   static constexpr int kBytes = kTmemSlot + 16;
 };
 
@@ -89,7 +91,18 @@ struct FwdBars {
   __device__ uint32_t go(int r) const {
     return base + 8 * (1 + kKSlots + kVSlots + 3 * kSRegions + r);
   }
+  __device__ uint32_t sched_full(int s) const {
+    return base + 8 * (1 + kKSlots + kVSlots + 4 * kSRegions + s);
+  }
+  __device__ uint32_t sched_empty(int s) const {
+    return base + 8 * (3 + kKSlots + kVSlots + 4 * kSRegions + s);
+  }
+  __device__ uint32_t o_free() const { return base + 8 * (5 + kKSlots + kVSlots + 4 * kSRegions); }
 };
+
+// Roles that read each published work item: the MMA issuer, the V producer,
+// the gatekeeper and softmax warp 0 (which shares it with the other seven).
+constexpr int kSchedReaders = 4;
 
 
 // The 256 softmax threads (both warpgroups).
@@ -144,7 +157,19 @@ __device__ __forceinline__ void tmem_cols_to_bf16(uint32_t taddr, bool live, flo
 
 // kShortLast: N is not a multiple of 128. kFp8 (d = 128 only): e4m3 Q, K and
 // transposed V with block scales, kind::f8f6f4 MMAs (K = 32 per instruction),
-// P stored as e4m3(p * 256).
+// P stored as e4m3(p * kFp8PScale).
+//
+// Persistent: one CTA per SM takes work items (one query block of one head)
+// from a global counter until none is left. The Q/K producer claims the items
+// and publishes them to the other roles through a two-entry ring in shared
+// memory. Every role numbers the key blocks it handles with one running step
+// index J across items, so the K, V and S rings, their barriers and the
+// tensor pipe run on from one item into the next: the next item's Q, first K
+// blocks and first S products are loaded and computed while the softmax warps
+// finish the current item. Two hand-offs cross an item boundary: Q is
+// reloaded once the last S of the previous item has completed, and the first
+// O += P V of an item (which overwrites O) waits until the softmax warps have
+// read the previous item's O out of TMEM (o_free).
 template <int D, bool kShortLast, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -154,17 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kOCols = D / 2;  // O columns per softmax warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // Work item: head-major, longest query blocks of each head first, so the
-  // CTAs that run together share one head's K and V in L2.
-  const int bh = blockIdx.x / p.Tr, rank = blockIdx.x % p.Tr;
-  const int b = bh / p.H, h = bh % p.H;
-  const int bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
-  const int r = p.row_order[static_cast<size_t>(bm) * p.Tr + rank];
-  const int ntiles = p.row_count[static_cast<size_t>(bm) * p.Tr + r];
-  const int32_t* list = p.row_list + (static_cast<size_t>(bm) * p.Tr + r) * p.Tc;
-  const int head_row0 = bh * p.N;           // first row of this head in [B*H*N, d]
-  const int q_row0 = head_row0 + r * kTile;  // first query row of the block
+  const int n_items = p.B * p.H * p.Tr;
 
   if ((smem_u32(smem) & 1023u) != 0) {  // 128-byte swizzle atoms need 1024-byte alignment
     if (tid == 0) record_failure(p.status, kStatusLayout, kSiteFwdSmemAlign);
@@ -173,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK),
                  sV = smem_u32(smem + L::kV);
   float* red = reinterpret_cast<float*>(smem + L::kRed);
+  // [0, 2): the item ring; [2, 4): the item as the softmax warps share it
+  volatile int* sched = reinterpret_cast<volatile int*>(smem + L::kSched);
   const FwdBars bar{smem_u32(smem + L::kBar)};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
@@ -190,6 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar.pv_done(g), 1);
       mbar_init(bar.go(g), 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar.sched_full(s), 1);
+      mbar_init(bar.sched_empty(s), kSchedReaders);
+    }
+    mbar_init(bar.o_free(), 8);
     fence_barrier_init();
   }
   tc_fence_before();
@@ -197,61 +219,133 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Work item n: head-major, longest query blocks of each head first, so the
+  // CTAs working at the same time share one head's K and V in L2.
+  struct Item {
+    int bh, bm, r, ntiles, head_row0, q_row0;
+    const int32_t* list;
+  };
+  auto decode = [&](int n) -> Item {
+    Item it;
+    it.bh = n / p.Tr;
+    const int rank = n % p.Tr;
+    const int b = it.bh / p.H, h = it.bh % p.H;
+    it.bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
+    it.r = p.row_order[static_cast<size_t>(it.bm) * p.Tr + rank];
+    it.ntiles = p.row_count[static_cast<size_t>(it.bm) * p.Tr + it.r];
+    it.list = p.row_list + (static_cast<size_t>(it.bm) * p.Tr + it.r) * p.Tc;
+    it.head_row0 = it.bh * p.N;               // first row of this head in [B*H*N, d]
+    it.q_row0 = it.head_row0 + it.r * kTile;  // first query row of the block
+    return it;
+  };
+  // The k-th item of this CTA (k = 0, 1, ...) from the ring, or -1 when no
+  // item is left or the wait gave up (then `ok` is false).
+  auto read_item = [&](int k, bool& ok) -> int {
+    const int s = k & 1;
+    if (!mbar_wait(bar.sched_full(s), (k >> 1) & 1, p.status)) {
+      record_failure(p.status, kStatusTimeout, kSiteFwdSched);
+      ok = false;
+      return -1;
+    }
+    const int n = sched[s];
+    mbar_arrive(bar.sched_empty(s));
+    return n;
+  };
+
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer of Q, K
-    if (lane == 0 && ntiles > 0) {
+    // ------------------------------------------------------------ scheduler, TMA producer of Q, K
+    if (lane == 0) {
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mk);
-      mbar_arrive_expect_tx(bar.q_full(), L::kTileBytes);
-      for (int ch = 0; ch < L::kChunks; ++ch)
-        tma_load_2d(sQ + ch * L::kChunk, &mq, ch * 64, q_row0, bar.q_full());
-      // K_j into slot j % 3 once S_{j-3} has completed
-      auto load_k = [&](int j) -> bool {
-        const int slot = j % kKSlots;
-        if (j >= kKSlots &&
-            !mbar_wait(bar.s_full(slot), ((j / kKSlots) - 1) & 1, p.status)) {
+      auto claim = [&]() -> int {
+        const int n = atomicAdd(p.sched, 1);
+        return n < n_items ? n : -1;
+      };
+      // K of step J into slot J % 3 once S_{J-3} has completed
+      auto load_k = [&](int J, int krow) -> bool {
+        const int slot = J % kKSlots;
+        if (J >= kKSlots &&
+            !mbar_wait(bar.s_full(slot), ((J / kKSlots) - 1) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteFwdKEmpty);
           return false;
         }
         mbar_arrive_expect_tx(bar.k_full(slot), L::kTileBytes);
-        const int krow = head_row0 + (list[j] >> 2) * kTile;
         for (int ch = 0; ch < L::kChunks; ++ch)
           tma_load_2d(sK + slot * L::kTileBytes + ch * L::kChunk, &mk, ch * 64, krow,
                       bar.k_full(slot));
         return true;
       };
+      int cur = claim();
+      sched[0] = cur;
+      mbar_arrive(bar.sched_full(0));
       bool ok = true;
-      for (int j = 0; ok && j < ntiles; ++j) ok = load_k(j);
-    }
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ TMA producer of V
-    if (lane == 0 && ntiles > 0) {
-      tma_prefetch_desc(&mv);
-      bool ok = true;
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int slot = j % kVSlots;
-        if (j >= kVSlots &&
-            !mbar_wait(bar.pv_done(slot), ((j / kVSlots) - 1) & 1, p.status)) {
-          record_failure(p.status, kStatusTimeout, kSiteFwdVEmpty);
+      int J = 0, J_last = -1;  // running step; last step of the previous item with tiles
+      for (int k = 0; ok && cur >= 0; ++k) {
+        const Item it = decode(cur);
+        if (it.ntiles > 0) {
+          // the Q buffer is free once the last S of the previous item is done
+          if (J_last >= 0 && !mbar_wait(bar.s_full(J_last % kSRegions),
+                                        (J_last / kSRegions) & 1, p.status)) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdKEmpty);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar.q_full(), L::kTileBytes);
+          for (int ch = 0; ch < L::kChunks; ++ch)
+            tma_load_2d(sQ + ch * L::kChunk, &mq, ch * 64, it.q_row0, bar.q_full());
+          for (int j = 0; ok && j < it.ntiles; ++j, ++J)
+            ok = load_k(J, it.head_row0 + (it.list[j] >> 2) * kTile);
+          J_last = J - 1;
+        }
+        // claim the next item once this one's loads are issued; its ring
+        // entry was last used by item k - 1, which every reader has taken
+        const int nxt = claim();
+        const int s = (k + 1) & 1;
+        if (k >= 1 && !mbar_wait(bar.sched_empty(s), ((k - 1) >> 1) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdSched);
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar.v_full(slot), L::kTileBytes);
-        if constexpr (kFp8) {
-          // V^T tile: the head's 128 rows of d, the block's 128 keys
-          tma_load_2d(sV + slot * L::kTileBytes, &mv, (list[j] >> 2) * kTile, bh * 128,
-                      bar.v_full(slot));
-        } else {
-          const int vrow = head_row0 + (list[j] >> 2) * kTile;
-          for (int ch = 0; ch < L::kChunks; ++ch)
-            tma_load_2d(sV + slot * L::kTileBytes + ch * L::kChunk, &mv, ch * 64, vrow,
+        sched[s] = nxt;
+        mbar_arrive(bar.sched_full(s));
+        cur = nxt;
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ TMA producer of V
+    if (lane == 0) {
+      tma_prefetch_desc(&mv);
+      bool ok = true;
+      int J = 0;
+      for (int k = 0; ok; ++k) {
+        const int n = read_item(k, ok);
+        if (n < 0) break;
+        const Item it = decode(n);
+        for (int j = 0; ok && j < it.ntiles; ++j, ++J) {
+          const int slot = J % kVSlots;
+          if (J >= kVSlots &&
+              !mbar_wait(bar.pv_done(slot), ((J / kVSlots) - 1) & 1, p.status)) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdVEmpty);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar.v_full(slot), L::kTileBytes);
+          if constexpr (kFp8) {
+            // V^T tile: the head's 128 rows of d, the block's 128 keys
+            tma_load_2d(sV + slot * L::kTileBytes, &mv, (it.list[j] >> 2) * kTile, it.bh * 128,
                         bar.v_full(slot));
+          } else {
+            const int vrow = it.head_row0 + (it.list[j] >> 2) * kTile;
+            for (int ch = 0; ch < L::kChunks; ++ch)
+              tma_load_2d(sV + slot * L::kTileBytes + ch * L::kChunk, &mv, ch * 64, vrow,
+                          bar.v_full(slot));
+          }
         }
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && ntiles > 0) {
+    if (lane == 0) {
       constexpr uint32_t idesc_s = kFp8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, 0, 1);
       constexpr int kSSteps = kFp8 ? D / 32 : D / 16;  // K steps of S = Q K^T
@@ -264,11 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk_base = sdesc_sw128(sK, 16, 1024);
       // V is MN-major [keys][d] in bf16, K-major [d][keys] as e4m3 V^T
       const uint64_t dv_base = kFp8 ? sdesc_sw128(sV, 16, 1024) : sdesc_sw128(sV, 16384, 1024);
-      // S_j; for j < 2 after waiting for K_j here, later ones after go(j - 2)
-      auto issue_s = [&](int j) -> bool {
-        const int slot = j % kKSlots, g = j % kSRegions;
-        if (j < 2) {
-          if (!mbar_wait(bar.k_full(slot), (j / kKSlots) & 1, p.status)) {
+      // S of step J; the first two steps of an item wait for their K here,
+      // later ones were cleared by the gatekeeper's go(J - 2)
+      auto issue_s = [&](int J, bool wait_k) -> bool {
+        const int slot = J % kKSlots, g = J % kSRegions;
+        if (wait_k) {
+          if (!mbar_wait(bar.k_full(slot), (J / kKSlots) & 1, p.status)) {
             record_failure(p.status, kStatusTimeout, kSiteFwdK);
             return false;
           }
@@ -284,54 +379,79 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             mma_ss(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, k > 0);
         }
-        mma_commit(bar.s_full(g));  // also frees K slot j % 3
+        mma_commit(bar.s_full(g));  // also frees K slot J % 3
         return true;
       };
-      bool ok = mbar_wait(bar.q_full(), 0, p.status);
-      if (!ok) record_failure(p.status, kStatusTimeout, kSiteFwdQ);
-      if (ok) ok = issue_s(0);
-      if (ok && ntiles > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int g = j % kSRegions, vs = j % kVSlots;
-        if (!mbar_wait(bar.go(g), (j / kSRegions) & 1, p.status)) {
-          record_failure(p.status, kStatusTimeout, kSiteFwdP);
+      bool ok = true;
+      int J = 0, ti = 0;  // running step; items with tiles so far
+      for (int k = 0; ok; ++k) {
+        const int n = read_item(k, ok);
+        if (n < 0) break;
+        const int ntiles = decode(n).ntiles;
+        if (ntiles == 0) continue;
+        if (!mbar_wait(bar.q_full(), ti & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdQ);
           break;
         }
         tc_fence_after();
-        const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
+        ok = issue_s(J, true);
+        if (ok && ntiles > 1) ok = issue_s(J + 1, true);
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int Jj = J + j, g = Jj % kSRegions, vs = Jj % kVSlots;
+          if (!mbar_wait(bar.go(g), (Jj / kSRegions) & 1, p.status)) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdP);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < kPvSteps; ++k) {
-          // A: P, 8 TMEM columns per K step; B: the next 16 key rows of V
-          // (bf16) or the next 32 key bytes of each row of V^T (e4m3)
-          if constexpr (kFp8)
-            mma_ts_f8(tmem + kColO, tmem + 128 * g + 8 * k,
-                      vd + static_cast<uint64_t>((k * 32) >> 4), idesc_pv, (j > 0 || k > 0));
-          else
-            mma_ts(tmem + kColO, tmem + 128 * g + 8 * k,
-                   vd + static_cast<uint64_t>((k * 2048) >> 4), idesc_pv, (j > 0 || k > 0));
+          for (int kk = 0; kk < kPvSteps; ++kk) {
+            // A: P, 8 TMEM columns per K step; B: the next 16 key rows of V
+            // (bf16) or the next 32 key bytes of each row of V^T (e4m3)
+            if constexpr (kFp8)
+              mma_ts_f8(tmem + kColO, tmem + 128 * g + 8 * kk,
+                        vd + static_cast<uint64_t>((kk * 32) >> 4), idesc_pv, (j > 0 || kk > 0));
+            else
+              mma_ts(tmem + kColO, tmem + 128 * g + 8 * kk,
+                     vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (j > 0 || kk > 0));
+          }
+          mma_commit(bar.pv_done(g));  // also frees V slot J % 3
+          if (j + 2 < ntiles) ok = issue_s(Jj + 2, false);  // cleared by go(J)
         }
-        mma_commit(bar.pv_done(g));  // also frees V slot j % 3
-        if (j + 2 < ntiles) issue_s(j + 2);  // its region and K slot are cleared by go(j)
+        J += ntiles;
+        ++ti;
       }
     }
   } else if (warp == 11) {
     // ------------------------------------------------------------ gatekeeper
-    if (lane == 0 && ntiles > 0) {
-      for (int j = 0; j < ntiles; ++j) {
-        const int g = j % kSRegions;
-        bool ok = true;
-        if (j + 2 < ntiles)
-          ok = mbar_wait(bar.k_full((j + 2) % kKSlots), ((j + 2) / kKSlots) & 1, p.status);
-        ok = ok && mbar_wait(bar.v_full(j % kVSlots), (j / kVSlots) & 1, p.status);
-        if (j >= 1)
-          ok = ok && mbar_wait(bar.pv_done((j - 1) % kSRegions), ((j - 1) / kSRegions) & 1,
-                               p.status);
-        ok = ok && mbar_wait(bar.p_full(g), (j / kSRegions) & 1, p.status);
-        if (!ok) {
-          record_failure(p.status, kStatusTimeout, kSiteFwdP);
-          break;
+    if (lane == 0) {
+      bool ok = true;
+      int J = 0, ti = 0;
+      for (int k = 0; ok; ++k) {
+        const int n = read_item(k, ok);
+        if (n < 0) break;
+        const int ntiles = decode(n).ntiles;
+        if (ntiles == 0) continue;
+        for (int j = 0; j < ntiles; ++j, ++J) {
+          const int g = J % kSRegions;
+          if (j + 2 < ntiles)
+            ok = mbar_wait(bar.k_full((J + 2) % kKSlots), ((J + 2) / kKSlots) & 1, p.status);
+          ok = ok && mbar_wait(bar.v_full(J % kVSlots), (J / kVSlots) & 1, p.status);
+          if (J >= 1)
+            ok = ok && mbar_wait(bar.pv_done((J - 1) % kSRegions), ((J - 1) / kSRegions) & 1,
+                                 p.status);
+          // the item's first O += P V overwrites O: the previous item's O must
+          // have been read out
+          if (j == 0 && ti > 0) ok = ok && mbar_wait(bar.o_free(), (ti - 1) & 1, p.status);
+          ok = ok && mbar_wait(bar.p_full(g), (J / kSRegions) & 1, p.status);
+          if (!ok) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdP);
+            break;
+          }
+          mbar_arrive(bar.go(g));
         }
-        mbar_arrive(bar.go(g));
+        ++ti;
       }
     }
   } else {
@@ -339,170 +459,198 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w = warp >> 2;                 // warpgroup: key columns [64w, 64w+64)
     const int row = (warp & 3) * 32 + lane;  // query row within the block = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // FP8: the true score is S times scale_Q(query block) * scale_K(key
-    // block); the product folds into each tile's exponent scale c
-    const float c_row = kFp8 ? p.scale_log2 * p.qscale[static_cast<size_t>(bh) * p.Tr + r]
-                             : p.scale_log2;
     constexpr float kThresh = kFp8 ? kRescaleThresholdFp8 : kRescaleThreshold;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    int next_entry = ntiles > 0 ? list[0] : 0;  // read one step ahead
-    // After a failed wait the warp keeps stepping through the loop without
-    // touching TMEM, so that both warpgroups pass the same named barriers and
+    // After a failed wait the warp keeps stepping through its items without
+    // touching TMEM, so that all eight warps pass the same named barriers and
     // the CTA can still reach its exit; `ok` is kept uniform across the warp.
-    for (int j = 0; j < ntiles; ++j) {
-      const int entry = next_entry;
-      if (j + 1 < ntiles) next_entry = list[j + 1];
-      const int g = j % kSRegions;
-      const float c =
-          kFp8 ? c_row * p.kscale[static_cast<size_t>(bh) * p.Tc + (entry >> 2)] : c_row;
-      // The element mask applies on PARTIAL tiles and on every tile of a short
-      // last key block (its keys >= N do not exist and are masked).
-      const bool short_keys = kShortLast && (entry >> 2) == p.Tc - 1;
-      const bool partial = (entry & 3) == FM_TILE_PARTIAL || short_keys;
-      // lane l builds the masked-row bits of key column 64w + 32k + l for this
-      // warp's 32 rows; a bit transpose hands each lane its own row's bits
-      // over those 32 columns. The bound loads overlap the wait for S.
-      uint32_t mbits[2] = {0u, 0u};
-      if (partial) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int jc = (entry >> 2) * kTile + 64 * w + 32 * k + lane;
-          uint32_t colbits = 0xffffffffu;  // a key >= N masks every row
-          if (!kShortLast || jc < p.N) {
-            const size_t col = static_cast<size_t>(bm) * p.N + jc;
-            const int lts = p.mask.lts[col], lte = p.mask.lte[col];
-            const int uts = p.mask.uts ? p.mask.uts[col] : 0;
-            const int ute = p.mask.ute ? p.mask.ute[col] : 0;
-            colbits = column_mask_bits(jc, lts, lte, uts, ute, p.mask.causal != 0,
-                                       r * kTile + 32 * (warp & 3));
-          }
-          mbits[k] = warp_transpose_bits(colbits);
-        }
+    bool ok = true;
+    int J = 0;  // running step
+    for (int k = 0;; ++k) {
+      // warp 0 takes the item from the ring and shares it through shared
+      // memory, so that the eight warps agree on it even after a failure
+      if (warp == 0 && lane == 0) {
+        bool okr = true;
+        sched[2 + (k & 1)] = read_item(k, okr);
       }
-      if (ok) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar.s_full(g), (j / kSRegions) & 1, p.status));
-        if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdS);
-      }
-      uint32_t sv[64];
-      float pm = -INFINITY;
-      if (ok) {
-        tc_fence_after();
-        const uint32_t s_addr = tmem + lane_base + 128 * g + 64 * w;
-        tmem_ld64(s_addr, s_addr + 32, sv);
+      softmax_bar();
+      const int n = sched[2 + (k & 1)];
+      if (n < 0) break;
+      const Item it = decode(n);
+      const int ntiles = it.ntiles, r = it.r, bh = it.bh, bm = it.bm;
+      // FP8: the true score is S times scale_Q(query block) * scale_K(key
+      // block); the product folds into each tile's exponent scale c
+      const float c_row = kFp8 ? p.scale_log2 * p.qscale[static_cast<size_t>(bh) * p.Tr + r]
+                               : p.scale_log2;
+      float m = -INFINITY, l = 0.f;
+      int next_entry = ntiles > 0 ? it.list[0] : 0;  // read one step ahead
+      for (int j = 0; j < ntiles; ++j) {
+        const int Jj = J + j;
+        const int entry = next_entry;
+        if (j + 1 < ntiles) next_entry = it.list[j + 1];
+        const int g = Jj % kSRegions;
+        const float c =
+            kFp8 ? c_row * p.kscale[static_cast<size_t>(bh) * p.Tc + (entry >> 2)] : c_row;
+        // The element mask applies on PARTIAL tiles and on every tile of a short
+        // last key block (its keys >= N do not exist and are masked).
+        const bool short_keys = kShortLast && (entry >> 2) == p.Tc - 1;
+        const bool partial = (entry & 3) == FM_TILE_PARTIAL || short_keys;
+        // lane l builds the masked-row bits of key column 64w + 32k + l for this
+        // warp's 32 rows; a bit transpose hands each lane its own row's bits
+        // over those 32 columns. The bound loads overlap the wait for S.
+        uint32_t mbits[2] = {0u, 0u};
         if (partial) {
 #pragma unroll
-          for (int jj = 0; jj < 64; ++jj)
-            sv[jj] = ((mbits[jj >> 5] >> (jj & 31)) & 1u) ? 0xff800000u : sv[jj];
+          for (int kk = 0; kk < 2; ++kk) {
+            const int jc = (entry >> 2) * kTile + 64 * w + 32 * kk + lane;
+            uint32_t colbits = 0xffffffffu;  // a key >= N masks every row
+            if (!kShortLast || jc < p.N) {
+              const size_t col = static_cast<size_t>(bm) * p.N + jc;
+              const int lts = p.mask.lts[col], lte = p.mask.lte[col];
+              const int uts = p.mask.uts ? p.mask.uts[col] : 0;
+              const int ute = p.mask.ute ? p.mask.ute[col] : 0;
+              colbits = column_mask_bits(jc, lts, lte, uts, ute, p.mask.causal != 0,
+                                         r * kTile + 32 * (warp & 3));
+            }
+            mbits[kk] = warp_transpose_bits(colbits);
+          }
         }
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+        if (ok) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar.s_full(g), (Jj / kSRegions) & 1, p.status));
+          if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdS);
+        }
+        uint32_t sv[64];
+        float pm = -INFINITY;
+        if (ok) {
+          tc_fence_after();
+          const uint32_t s_addr = tmem + lane_base + 128 * g + 64 * w;
+          tmem_ld64(s_addr, s_addr + 32, sv);
+          if (partial) {
 #pragma unroll
-        for (int jj = 0; jj < 64; jj += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sv[jj]));
-          mx1 = fmaxf(mx1, __uint_as_float(sv[jj + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sv[jj + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sv[jj + 3]));
-        }
-        pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
-      }
-      // exchange the two partial row maxima (double-buffered by step parity);
-      // the barrier also orders both warpgroups' S loads before any P store
-      // into the region
-      red[((j & 1) * 2 + w) * kTile + row] = pm;
-      softmax_bar();
-      if (ok) {
-        const float mx = fmaxf(pm, red[((j & 1) * 2 + (w ^ 1)) * kTile + row]);
-        const float m_new = fmaxf(m, mx);
-        const bool rescale = m_new > m + kThresh;
-        float alpha = 1.f;
-        if (rescale) {
-          alpha = ex2(m - m_new);
-          m = m_new;
-        }
-        const float m_use = (m == -INFINITY) ? 0.f : m;
-        // pairs of columns through the paired fp32 instructions: s * c - m
-        // and the running pair of partial sums take one issue slot per pair
-        const uint64_t c2 = f2_make(c, c), nm2 = f2_make(-m_use, -m_use);
-        uint64_t l2 = f2_make(0.f, 0.f);
-        uint32_t pk[32];  // bf16 pairs; FP8: e4m3 quads in pk[0..15]
-        float pq0 = 0.f, pq1 = 0.f;
+            for (int jj = 0; jj < 64; ++jj)
+              sv[jj] = ((mbits[jj >> 5] >> (jj & 31)) & 1u) ? 0xff800000u : sv[jj];
+          }
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float x0, x1;
-          f2_split(f2_fma(f2_make(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), c2,
-                          nm2),
-                   x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          l2 = f2_add(l2, f2_make(p0, p1));
+          for (int jj = 0; jj < 64; jj += 4) {
+            mx0 = fmaxf(mx0, __uint_as_float(sv[jj]));
+            mx1 = fmaxf(mx1, __uint_as_float(sv[jj + 1]));
+            mx2 = fmaxf(mx2, __uint_as_float(sv[jj + 2]));
+            mx3 = fmaxf(mx3, __uint_as_float(sv[jj + 3]));
+          }
+          pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+        }
+        // exchange the two partial row maxima (double-buffered by step parity);
+        // the barrier also orders both warpgroups' S loads before any P store
+        // into the region
+        red[((Jj & 1) * 2 + w) * kTile + row] = pm;
+        softmax_bar();
+        if (ok) {
+          const float mx = fmaxf(pm, red[((Jj & 1) * 2 + (w ^ 1)) * kTile + row]);
+          const float m_new = fmaxf(m, mx);
+          const bool rescale = m_new > m + kThresh;
+          float alpha = 1.f;
+          if (rescale) {
+            alpha = ex2(m - m_new);
+            m = m_new;
+          }
+          const float m_use = (m == -INFINITY) ? 0.f : m;
+          // pairs of columns through the paired fp32 instructions: s * c - m
+          // and the running pair of partial sums take one issue slot per pair
+          const uint64_t c2 = f2_make(c, c), nm2 = f2_make(-m_use, -m_use);
+          uint64_t l2 = f2_make(0.f, 0.f);
+          uint32_t pk[32];  // bf16 pairs; FP8: e4m3 quads in pk[0..15]
+          float pq0 = 0.f, pq1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float x0, x1;
+            f2_split(f2_fma(f2_make(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
+                            c2, nm2),
+                     x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            l2 = f2_add(l2, f2_make(p0, p1));
+            if constexpr (kFp8) {
+              // the scale keeps small probabilities above e4m3's subnormal range
+              if (i & 1)
+                pk[i >> 1] = pack_e4m3x4(pq0, pq1, p0 * kFp8PScale, p1 * kFp8PScale);
+              else
+                pq0 = p0 * kFp8PScale, pq1 = p1 * kFp8PScale;
+            } else {
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+          }
+          float l0, l1;
+          f2_split(l2, l0, l1);
+          l = l * alpha + (l0 + l1);
+          // P_j over this warpgroup's part of S_j's region: keys [64w, 64w+64)
+          // as bf16 pairs in columns [32w, 32w+32) (the A operand of P V)
           if constexpr (kFp8) {
-            // the scale keeps small probabilities above e4m3's subnormal range
-            if (i & 1)
-              pk[i >> 1] = pack_e4m3x4(pq0, pq1, p0 * kFp8PScale, p1 * kFp8PScale);
-            else
-              pq0 = p0 * kFp8PScale, pq1 = p1 * kFp8PScale;
+            // ... or as e4m3 quads in columns [16w, 16w+16)
+            tmem_st16(tmem + lane_base + 128 * g + 16 * w,
+                      *reinterpret_cast<const uint32_t(*)[16]>(pk));
           } else {
-            pk[i] = pack_bf16x2(p0, p1);
+            tmem_st32p(tmem + lane_base + 128 * g + 32 * w, pk);
           }
-        }
-        float l0, l1;
-        f2_split(l2, l0, l1);
-        l = l * alpha + (l0 + l1);
-        // P_j over this warpgroup's part of S_j's region: keys [64w, 64w+64)
-        // as bf16 pairs in columns [32w, 32w+32) (the A operand of P V)
-        if constexpr (kFp8) {
-          // ... or as e4m3 quads in columns [16w, 16w+16)
-          tmem_st16(tmem + lane_base + 128 * g + 16 * w,
-                    *reinterpret_cast<const uint32_t(*)[16]>(pk));
-        } else {
-          tmem_st32p(tmem + lane_base + 128 * g + 32 * w, pk);
-        }
-        if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-          // O is rescaled once O += P_{j-1} V_{j-1} has completed
-          ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done((j - 1) % kSRegions),
-                                                 ((j - 1) / kSRegions) & 1, p.status));
-          if (ok) {
-            tc_fence_after();
+          if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+            // O is rescaled once O += P_{j-1} V_{j-1} has completed
+            ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done((Jj - 1) % kSRegions),
+                                                   ((Jj - 1) / kSRegions) & 1, p.status));
+            if (ok) {
+              tc_fence_after();
 #pragma unroll
-            for (int ch = 0; ch < kOCols / 32; ++ch)
-              tmem_scale_cols<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, alpha);
-          } else if (lane == 0) {
-            record_failure(p.status, kStatusTimeout, kSiteFwdO);
+              for (int ch = 0; ch < kOCols / 32; ++ch)
+                tmem_scale_cols<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, alpha);
+            } else if (lane == 0) {
+              record_failure(p.status, kStatusTimeout, kSiteFwdO);
+            }
           }
+          tmem_st_wait();
         }
-        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.p_full(g));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.p_full(g));
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && ntiles > 0) {
-      const int jl = ntiles - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(jl % kSRegions), (jl / kSRegions) & 1,
-                                             p.status));
-      if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdO);
-      tc_fence_after();
-    }
-    // row sums through the exchange buffer of the parity the last step did not
-    // use (its previous readers passed the last step's barrier)
-    float* lsum = red + (ntiles & 1) * 2 * kTile;
-    lsum[w * kTile + row] = l;
-    softmax_bar();
-    const float ltot = l + lsum[(w ^ 1) * kTile + row];
-    const bool live = ok && ntiles > 0;
-    const bool has = live && ltot > 0.f;
-    // FP8: O accumulated (kFp8PScale P) (V / scale_V)
-    const float inv = has ? (kFp8 ? p.vscale[bh] * (1.f / kFp8PScale) : 1.f) / ltot : 0.f;
-    // rows >= N of a short last query block do not exist: nothing is stored
-    const bool row_exists = !kShortLast || r * kTile + row < p.N;
-    uint16_t* orow = p.o + static_cast<size_t>(q_row0 + row) * D + w * kOCols;
+      // ---------------------------------------------------------- epilogue of the item
+      if (ok && ntiles > 0) {
+        const int jl = J + ntiles - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(jl % kSRegions),
+                                               (jl / kSRegions) & 1, p.status));
+        if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdO);
+        tc_fence_after();
+      }
+      // row sums through the exchange buffer of the parity the item's last
+      // step did not use (its readers passed that step's barrier)
+      float* lsum = red + ((J + ntiles) & 1) * 2 * kTile;
+      lsum[w * kTile + row] = l;
+      softmax_bar();
+      const float ltot = l + lsum[(w ^ 1) * kTile + row];
+      const bool live = ok && ntiles > 0;
+      const bool has = live && ltot > 0.f;
+      // FP8: O accumulated (kFp8PScale P) (V / scale_V)
+      const float inv = has ? (kFp8 ? p.vscale[bh] * (1.f / kFp8PScale) : 1.f) / ltot : 0.f;
+      // rows >= N of a short last query block do not exist: nothing is stored
+      const bool row_exists = !kShortLast || r * kTile + row < p.N;
+      uint16_t* orow = p.o + static_cast<size_t>(it.q_row0 + row) * D + w * kOCols;
 #pragma unroll
-    for (int ch = 0; ch < kOCols / 32; ++ch)
-      tmem_cols_to_bf16<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, live, inv,
-                            orow + 32 * ch, row_exists);
-    if (w == 0 && row_exists) {
-      const float m_fin = (m == -INFINITY) ? 0.f : m;
-      p.lse[q_row0 + row] = has ? (m_fin + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
+      for (int ch = 0; ch < kOCols / 32; ++ch)
+        tmem_cols_to_bf16<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, live, inv,
+                              orow + 32 * ch, row_exists);
+      if (ntiles > 0) {
+        // O has been read (the loads above completed): the next item's first
+        // O += P V may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.o_free());
+      }
+      if (w == 0 && row_exists) {
+        const float m_fin = (m == -INFINITY) ? 0.f : m;
+        p.lse[it.q_row0 + row] =
+            has ? (m_fin + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
+      }
+      J += ntiles;
+      // every warp has read lsum before the next item's first step (or
+      // epilogue) writes the same buffer
+      softmax_bar();
     }
   }
 
@@ -521,7 +669,12 @@ cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kShortLast, kFp8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(p.B * p.H * p.Tr);
+  // persistent: one CTA per SM (at most one per work item); the item counter
+  // starts at zero
+  const int items = p.B * p.H * p.Tr;
+  const unsigned grid = static_cast<unsigned>(items < p.num_sms ? items : p.num_sms);
+  e = cudaMemsetAsync(p.sched, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
   fwd_kernel<D, kShortLast, kFp8><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }

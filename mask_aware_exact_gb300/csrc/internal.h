@@ -15,7 +15,7 @@ enum : int { kStatusTimeout = 1, kStatusLayout = 2 };
 enum Site : int {
   kSiteNone = 0,
   kSiteFwdQ = 101, kSiteFwdK, kSiteFwdV, kSiteFwdS, kSiteFwdP, kSiteFwdO, kSiteFwdKEmpty,
-  kSiteFwdVEmpty, kSiteFwdSmemAlign,
+  kSiteFwdVEmpty, kSiteFwdSmemAlign, kSiteFwdSched,
   kSiteBwdKV = 201, kSiteBwdQ, kSiteBwdQEmpty, kSiteBwdS, kSiteBwdDP, kSiteBwdPT, kSiteBwdDS,
   kSiteBwdDV, kSiteBwdDQ, kSiteBwdDrained, kSiteBwdDone, kSiteBwdSmemAlign,
   kSiteSelftest = 301,
@@ -68,6 +68,8 @@ struct FwdParams {
   uint16_t* o;  // bf16 [B,H,N,d]
   float* lse;   // [B,H,N]
   int32_t* status;
+  int32_t* sched;  // work-item counter (zeroed by the launch)
+  int num_sms;     // persistent grid size
 };
 
 struct BwdParams {
