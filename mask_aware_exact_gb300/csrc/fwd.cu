@@ -5,31 +5,32 @@
 // work, and block-wise matmul interleaved with softmax).
 //
 // The non-FULL key blocks of the query block are visited one per step. The
-// tensor cores run ahead of the softmax: S_{j+2} = Q K_{j+2}^T is issued right
-// after O += P_j V_j, into one of three TMEM S regions, so that while the
-// softmax warps work on S_j the tensor pipe computes O += P_{j-1} V_{j-1} and
-// S_{j+1}. P_j is written as bf16 over S_j's own region.
+// tensor cores run ahead of the softmax: S_{j+3} = Q K_{j+3}^T is issued as
+// soon as O += P_j V_j (the last reader of its TMEM region) has completed, so
+// the S products stay off the chain softmax_j -> O += P_j V_j, and the
+// softmax warps find S_{j+1} ready when they finish step j. P_j is written
+// over S_j's own region.
 //
-// One CTA = one (batch, head, query block). Warp roles (320 threads):
+// Persistent CTAs (one per SM) take query blocks from a work counter; see the
+// kernel's comment. Warp roles (384 threads):
 //   warps 0-7  softmax, two warpgroups. Thread (w, r) owns query row r (= TMEM
 //              lane r) and key columns [64w, 64w+64) of every block: it loads
 //              its 64 S values into registers, applies the element mask on
 //              PARTIAL tiles, exchanges its partial row maximum with the other
 //              warpgroup through shared memory, keeps the running max and
-//              partial sum in fp32 (log2 domain), and writes its bf16 P slice
-//              into TMEM. O is rescaled only when the max grows by more than 2^8
+//              partial sum in fp32 (log2 domain), and writes its P slice into
+//              TMEM. O is rescaled only when the max grows by more than 2^8
 //              (lazy rescaling: exact after the final division); warpgroup w
 //              rescales O columns [w d/2, (w+1) d/2). Finally O = acc / l and LSE.
-//   warp 8     TMA producer of Q (once) and K blocks (three-slot ring).
-//   warp 9     MMA issuer (one thread): S_0, S_1, then per step O += P_j V_j and
-//              S_{j+2} back to back after a single wait. An MMA issue returns
-//              only when the tensor pipe takes the instruction, and every
-//              mbarrier wait or commit in this thread leaves the pipe idle, so
-//              the thread waits once per step.
+//   warp 8     work scheduler and TMA producer of Q (once per item) and K
+//              blocks (three-slot ring).
+//   warp 9     MMA issuer (one thread): per step O += P_j V_j after go(j), then
+//              S_{j+3} once that product has completed and K_{j+3} has landed.
 //   warp 10    TMA producer of V blocks (three-slot ring).
-//   warp 11    gatekeeper (one thread): for step j waits until K_{j+2} and V_j
-//              have landed, O += P_{j-1} V_{j-1} has completed (S_{j+2} reuses
-//              that region) and P_j is written, then signals go(j).
+//   warp 11    gatekeeper (one thread): for step j waits until V_j has landed,
+//              P_j is written (and, at an item's first step, the previous O
+//              has been read out), then signals go(j), so that the MMA thread
+//              waits once per product.
 //
 // TMEM columns (512 allocated): S regions [0,128) [128,256) [256,384), O [384, 384+d).
 // Ordering: S_{j+3} reuses the region of S_j / P_j once O += P_j V_j has
@@ -358,17 +359,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk_base = sdesc_sw128(sK, 16, 1024);
       // V is MN-major [keys][d] in bf16, K-major [d][keys] as e4m3 V^T
       const uint64_t dv_base = kFp8 ? sdesc_sw128(sV, 16, 1024) : sdesc_sw128(sV, 16384, 1024);
-      // S of step J; the first two steps of an item wait for their K here,
-      // later ones were cleared by the gatekeeper's go(J - 2)
-      auto issue_s = [&](int J, bool wait_k) -> bool {
+      // S of step J into region J % 3 once K_J has landed and O += P V of
+      // step J - 3 (the last reader of that region) has completed
+      auto issue_s = [&](int J) -> bool {
         const int slot = J % kKSlots, g = J % kSRegions;
-        if (wait_k) {
-          if (!mbar_wait(bar.k_full(slot), (J / kKSlots) & 1, p.status)) {
-            record_failure(p.status, kStatusTimeout, kSiteFwdK);
-            return false;
-          }
-          tc_fence_after();
+        if (J >= kSRegions &&
+            !mbar_wait(bar.pv_done(g), ((J / kSRegions) - 1) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdO);
+          return false;
         }
+        if (!mbar_wait(bar.k_full(slot), (J / kKSlots) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdK);
+          return false;
+        }
+        tc_fence_after();
         const uint64_t kd = dk_base + static_cast<uint64_t>((slot * L::kTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < kSSteps; ++k) {
@@ -394,8 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        ok = issue_s(J, true);
-        if (ok && ntiles > 1) ok = issue_s(J + 1, true);
+        // S runs three steps ahead of O += P V: the item's first three now,
+        // then S_{J+3} right after O += P_J V_J (same region) has completed,
+        // which keeps S off the softmax -> P V chain
+        for (int m = 0; ok && m < kSRegions && m < ntiles; ++m) ok = issue_s(J + m);
         for (int j = 0; ok && j < ntiles; ++j) {
           const int Jj = J + j, g = Jj % kSRegions, vs = Jj % kVSlots;
           if (!mbar_wait(bar.go(g), (Jj / kSRegions) & 1, p.status)) {
@@ -417,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (j > 0 || kk > 0));
           }
           mma_commit(bar.pv_done(g));  // also frees V slot J % 3
-          if (j + 2 < ntiles) ok = issue_s(Jj + 2, false);  // cleared by go(J)
+          if (j + kSRegions < ntiles) ok = issue_s(Jj + kSRegions);
         }
         J += ntiles;
         ++ti;
@@ -435,12 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ntiles == 0) continue;
         for (int j = 0; j < ntiles; ++j, ++J) {
           const int g = J % kSRegions;
-          if (j + 2 < ntiles)
-            ok = mbar_wait(bar.k_full((J + 2) % kKSlots), ((J + 2) / kKSlots) & 1, p.status);
-          ok = ok && mbar_wait(bar.v_full(J % kVSlots), (J / kVSlots) & 1, p.status);
-          if (J >= 1)
-            ok = ok && mbar_wait(bar.pv_done((J - 1) % kSRegions), ((J - 1) / kSRegions) & 1,
-                                 p.status);
+          ok = mbar_wait(bar.v_full(J % kVSlots), (J / kVSlots) & 1, p.status);
           // the item's first O += P V overwrites O: the previous item's O must
           // have been read out
           if (j == 0 && ti > 0) ok = ok && mbar_wait(bar.o_free(), (ti - 1) & 1, p.status);
