@@ -53,7 +53,7 @@ E2E_CHUNK_HEADS = 2
 
 NCU_TRAFFIC = {
     "bwd_main@3a87d70f205c@document_b1h32n32768d128": 4 * (405.988096e6 + 220.376832e6),
-    "fwd@876944492112@document_b1h32n32768d128": 4 * (201.910016e6 + 50.058752e6),
+    "fwd@176d56817e16@document_b1h32n32768d128": 4 * (201.946624e6 + 49.924608e6),
 }
 
 
