@@ -58,8 +58,8 @@ struct BwdLayout {
   static constexpr int kDelta = kLse + 2 * kTile * 4;   // fp32[2][128]
   static constexpr int kBar = kDelta + 2 * kTile * 4;
   // kv_full, q_full[2], q_empty[2], s_full, dp_full, pt_ready, ds_ready, dv_done,
-  // tile_done, dq_drained
-  static constexpr int kNumBars = 12;
+  // tile_done, dq_drained, do_full[2], do_empty[2]
+  static constexpr int kNumBars = 16;
   static constexpr int kTmemSlot = kBar + kNumBars * 8;
   static constexpr int kBytes = kTmemSlot + 16;
 };
@@ -76,6 +76,8 @@ struct BwdBars {
   __device__ uint32_t dv_done() const { return base + 8 * 9; }
   __device__ uint32_t tile_done() const { return base + 8 * 10; }
   __device__ uint32_t dq_drained() const { return base + 8 * 11; }
+  __device__ uint32_t do_full(int s) const { return base + 8 * (12 + s); }
+  __device__ uint32_t do_empty(int s) const { return base + 8 * (14 + s); }
 };
 
 
@@ -102,6 +104,10 @@ __device__ __forceinline__ void bulk_commit_group() {
 }
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// all but the most recent bulk group have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -205,6 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar.q_full(s), 1);
       mbar_init(bar.q_empty(s), 1);
+      mbar_init(bar.do_full(s), 1);
+      mbar_init(bar.do_empty(s), 1);
     }
     mbar_init(bar.s_full(), 1);
     mbar_init(bar.dp_full(), 1);
@@ -235,20 +243,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < ntiles; ++t) {
         const int st = t & 1;
         const int q_row = head_row0 + (list[t] >> 2) * kTile;
+        // lse2 and D live in the padded [B*H, Npad] workspace arrays
+        const size_t prow = static_cast<size_t>(bh) * p.Npad + (list[t] >> 2) * kTile;
+        // Q and lse2 of stage st (freed once the dQ boxes staged in the Q
+        // buffer two tiles earlier have been read by the bulk reduce) ...
         if (t >= 2 && !mbar_wait(bar.q_empty(st), ((t >> 1) - 1) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteBwdQEmpty);
           break;
         }
-        mbar_arrive_expect_tx(bar.q_full(st), 2 * L::kTileBytes + 2 * kTile * 4);
-        for (int ch = 0; ch < L::kChunks; ++ch) {
+        mbar_arrive_expect_tx(bar.q_full(st), L::kTileBytes + kTile * 4);
+        for (int ch = 0; ch < L::kChunks; ++ch)
           tma_load_2d(sQ + st * L::kTileBytes + ch * 16384, &mq, ch * 64, q_row, bar.q_full(st));
-          tma_load_2d(sDO + st * L::kTileBytes + ch * 16384, &mdo, ch * 64, q_row,
-                      bar.q_full(st));
-        }
-        // lse2 and D live in the padded [B*H, Npad] workspace arrays
-        const size_t prow = static_cast<size_t>(bh) * p.Npad + (list[t] >> 2) * kTile;
         bulk_load(smem_u32(lse_s + st * kTile), p.lse2 + prow, kTile * 4, bar.q_full(st));
-        bulk_load(smem_u32(delta_s + st * kTile), p.delta + prow, kTile * 4, bar.q_full(st));
+        // ... then dO and D (freed when the boxes staged in the dO buffer have
+        // been read), so that S and P of a tile can start before its dO lands
+        if (t >= 2 && !mbar_wait(bar.do_empty(st), ((t >> 1) - 1) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteBwdQEmpty);
+          break;
+        }
+        mbar_arrive_expect_tx(bar.do_full(st), L::kTileBytes + kTile * 4);
+        for (int ch = 0; ch < L::kChunks; ++ch)
+          tma_load_2d(sDO + st * L::kTileBytes + ch * 16384, &mdo, ch * 64, q_row,
+                      bar.do_full(st));
+        bulk_load(smem_u32(delta_s + st * kTile), p.delta + prow, kTile * 4, bar.do_full(st));
       }
     }
   } else if (warp == 13) {
@@ -288,6 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar.s_full());
         if (t >= 1 && !mbar_wait(bar.dq_drained(), (t - 1) & 1, p.status)) {  // dQ_{t-1} read out
           record_failure(p.status, kStatusTimeout, kSiteBwdDrained);
+          break;
+        }
+        if (!mbar_wait(bar.do_full(st), (t >> 1) & 1, p.status)) {  // dO_t landed
+          record_failure(p.status, kStatusTimeout, kSiteBwdQ);
           break;
         }
         tc_fence_after();
@@ -405,6 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
+      if (!mbar_wait(bar.do_full(st), (t >> 1) & 1, p.status)) {  // D of this tile landed
+        record_failure(p.status, kStatusTimeout, kSiteBwdDP);
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const float* dl = delta_s + st * kTile + 64 * g;
       // row j of dS^T, queries [64g, 64g+64): the 128-byte row of chunk g, in
@@ -508,16 +534,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       drain_bar();
       if (leader) {
+        // the boxes staged in the Q buffer form one bulk group and those in
+        // the dO buffer a second, so that the Q buffer returns to the
+        // producer as soon as the first group has been read
+        constexpr int kQBoxes = L::kTileBytes / 16384;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
-          const uint32_t box = (ch * 16384 < L::kTileBytes)
+          const uint32_t box = (ch < kQBoxes)
                                    ? sQ + st * L::kTileBytes + ch * 16384
-                                   : sDO + st * L::kTileBytes + ch * 16384 - L::kTileBytes;
+                                   : sDO + st * L::kTileBytes + (ch - kQBoxes) * 16384;
           tma_reduce_add_2d(&mdq, box, ch * 32, bh * p.Npad + qb * kTile);
+          if (ch == kQBoxes - 1) bulk_commit_group();
         }
         bulk_commit_group();
-        bulk_wait_read_all();  // the stage buffers may be refilled now
+        bulk_wait_read_1();  // the Q-buffer group has been read
         if (t + 2 < ntiles) mbar_arrive(bar.q_empty(st));
+        bulk_wait_read_all();
+        if (t + 2 < ntiles) mbar_arrive(bar.do_empty(st));
       }
     }
     if (leader) bulk_wait_all();
