@@ -52,7 +52,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 E2E_CHUNK_HEADS = 2
 
 NCU_TRAFFIC = {
-    "bwd_main@3a87d70f205c@document_b1h32n32768d128": 4 * (405.988096e6 + 220.376832e6),
+    "bwd_main@172b1ff61d70@document_b1h32n32768d128": 4 * (405.954048e6 + 220.839424e6),
     "fwd@176d56817e16@document_b1h32n32768d128": 4 * (201.946624e6 + 49.924608e6),
 }
 
