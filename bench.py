@@ -272,6 +272,39 @@ def run_native(args):
     e2e_agg = R.aggregate_throughput(fl["total"] * K2, e2e_s, dev)
     del hws
 
+    # ---------------- FP8 forward (e4m3 block quantisation, quantisation
+    # included) on the same device inputs, timed after the step; reported
+    # beside the bf16 forward, never part of the headline
+    fp8 = None
+    if d == 128:
+        try:
+            ws8 = fm.alloc_fp8_workspace(B, H, Hm, N, device=dev)
+            fm.flashmask_classify(mask, B, N, ws8)
+
+            def fp8_fwd():
+                fm.flashmask_fwd_fp8(q, k, v, mask, ws8, scale=scale, o=o, lse=lse,
+                                     ws_classified=True)
+
+            for _ in range(args.warmup):
+                fp8_fwd()
+            K3 = max(3, K // 4)
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            b0.record(stream)
+            for _ in range(K3):
+                fp8_fwd()
+            b1.record(stream)
+            torch.cuda.synchronize()
+            st8, _ = fm.flashmask_check_status(ws8)
+            ms8 = b0.elapsed_time(b1) / K3
+            fp8 = {"api": "flashmask_fwd_fp8", "ms": round(ms8, 4),
+                   "tflops": round(fl["fwd"] / (ms8 / 1e3) / 1e12, 1),
+                   "bf16_fwd_ms": round(per["fwd"], 4), "quantisation_included": True,
+                   "calls": K3, "status": int(st8)}
+            del ws8
+        except Exception as e:  # reported, never fatal to the headline
+            fp8 = {"api": "flashmask_fwd_fp8", "error": str(e)[:200]}
+
     pk, pk_src = peaks()
     peak_dense = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     peak_sust = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
@@ -323,6 +356,8 @@ def run_native(args):
             "gpu_launches": 7 * K,
             "clocks": clk,
         }
+        if fp8 is not None:
+            result["fp8_forward"] = fp8
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(w, args.oracle_seconds)
     R.finalize()
