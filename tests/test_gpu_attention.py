@@ -243,3 +243,31 @@ def test_classification_reused_across_layers():
         check_forward(to_np(o), to_np(lse), o_ref, lse_ref, f"layer {layer}")
     st, site = fm.flashmask_check_status(ws)
     assert st == fm.FM_OK, (st, site)
+
+
+def test_forwards_on_two_streams_with_their_own_workspaces():
+    # the persistent forward takes its work items from a counter in the
+    # workspace: two forwards in flight at once on two streams, each with its
+    # own workspace, must not take each other's items
+    fm = need_gpu()
+    B, H, N, d = 1, 8, 2048, 128
+    specs = [W.document_bounds(B, 1, [700, 900, 448]), W.causal_bounds(B, 1, N)]
+    inputs = [W.make_qkv(B, H, N, d, seed=60 + i)[:3] for i in range(2)]
+    masks = [fm.DeviceMask.from_spec(s) for s in specs]
+    wss = [fm.alloc_workspace(B, H, 1, N, d, for_bwd=False) for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    dev_in = [[x.cuda() for x in qkv] for qkv in inputs]
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):  # several rounds, so the two grids overlap on the device
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                outs.append((i, fm.flashmask_fwd(*dev_in[i], masks[i], wss[i],
+                                                 stream=streams[i])))
+    torch.cuda.synchronize()
+    for i in range(2):
+        st, site = fm.flashmask_check_status(wss[i])
+        assert st == fm.FM_OK, (i, st, site)
+    refs = [A.forward(*inputs[i], specs[i], 1 / math.sqrt(d)) for i in range(2)]
+    for i, (o, lse) in outs:
+        check_forward(to_np(o), to_np(lse), refs[i][0], refs[i][1], f"stream {i}")
