@@ -248,15 +248,29 @@ def test_classification_reused_across_layers():
 def test_forwards_on_two_streams_with_their_own_workspaces():
     # the persistent forward takes its work items from a counter in the
     # workspace: two forwards in flight at once on two streams, each with its
-    # own workspace, must not take each other's items
+    # own workspace, must not take each other's items. Each item's arithmetic
+    # does not depend on which CTA runs it, so the results must be bit-equal
+    # to the same two forwards run one after the other; V is halved so that
+    # |O| stays below 4, where bf16 output rounding (half an ulp <= 2^-7)
+    # keeps within the absolute O tolerance against the oracle.
     fm = need_gpu()
     B, H, N, d = 1, 8, 2048, 128
     specs = [W.document_bounds(B, 1, [700, 900, 448]), W.causal_bounds(B, 1, N)]
-    inputs = [W.make_qkv(B, H, N, d, seed=60 + i)[:3] for i in range(2)]
+    inputs = []
+    for i in range(2):
+        q, k, v, _ = W.make_qkv(B, H, N, d, seed=60 + i)
+        inputs.append((q, k, (v.float() * 0.5).to(torch.bfloat16)))
     masks = [fm.DeviceMask.from_spec(s) for s in specs]
+    dev_in = [[x.cuda() for x in qkv] for qkv in inputs]
+    # one after the other on the current stream
+    seq = []
+    for i in range(2):
+        ws = fm.alloc_workspace(B, H, 1, N, d, for_bwd=False)
+        o, lse = fm.flashmask_fwd(*dev_in[i], masks[i], ws)
+        seq.append((o.clone(), lse.clone()))
+    # in flight together on two streams
     wss = [fm.alloc_workspace(B, H, 1, N, d, for_bwd=False) for _ in range(2)]
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
-    dev_in = [[x.cuda() for x in qkv] for qkv in inputs]
     torch.cuda.synchronize()
     outs = []
     for rep in range(3):  # several rounds, so the two grids overlap on the device
@@ -268,6 +282,9 @@ def test_forwards_on_two_streams_with_their_own_workspaces():
     for i in range(2):
         st, site = fm.flashmask_check_status(wss[i])
         assert st == fm.FM_OK, (i, st, site)
-    refs = [A.forward(*inputs[i], specs[i], 1 / math.sqrt(d)) for i in range(2)]
     for i, (o, lse) in outs:
-        check_forward(to_np(o), to_np(lse), refs[i][0], refs[i][1], f"stream {i}")
+        assert torch.equal(o, seq[i][0]), f"stream {i}: O differs from the sequential run"
+        assert torch.equal(lse, seq[i][1]), f"stream {i}: LSE differs from the sequential run"
+    for i in range(2):
+        o_ref, lse_ref = A.forward(*inputs[i], specs[i], 1 / math.sqrt(d))
+        check_forward(to_np(seq[i][0]), to_np(seq[i][1]), o_ref, lse_ref, f"forward {i}")
