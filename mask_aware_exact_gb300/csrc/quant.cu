@@ -13,7 +13,7 @@
 //   quant_qk_kernel  Q and K blocks -> codes and block scales; the V block's
 //                    absolute maximum folded into the head's with an atomic max
 //   quant_vt_kernel  V block -> codes with the head's scale, transposed through
-//                    shared memory
+//                    shared memory as packed 32-bit words
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -123,35 +123,47 @@ __global__ void __launch_bounds__(kQThreads) quant_qk_kernel(
 
 // V (bf16 [head][N][128]) -> Vt8 (e4m3 [head][128][Npad]) with the head's
 // scale; one CTA per (head, 128-key block). Keys >= N are written as 0.
+// Thread (key group kg, column group m) converts keys 4kg .. 4kg+3 at
+// columns 8m .. 8m+7 (four coalesced 16-byte loads: 16 threads cover one
+// 256-byte row) and stores the transposed bytes as eight 32-bit words, one
+// per column, each holding its four keys.
 __global__ void __launch_bounds__(kQThreads) quant_vt_kernel(
     const uint16_t* __restrict__ v, int N, int Npad, int Tr,
-    const unsigned int* __restrict__ vamax, uint8_t* __restrict__ vt8,
+    const unsigned int* __restrict__ amax, uint8_t* __restrict__ vt8,
     float* __restrict__ vscale) {
-  constexpr int kRow = 128 + 4;  // bytes per d row of the tile (padding shifts banks)
-  __shared__ __align__(16) uint8_t tile[128 * kRow];  // [d][key]
+  constexpr int kRowWords = 128 / 4 + 1;  // 32-bit words per d row of the tile (+1: banks)
+  __shared__ uint32_t tile[128 * kRowWords];  // [d][key / 4]
   const int bh = blockIdx.x / Tr, kb = blockIdx.x % Tr;
-  const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(kb) * kTile;
-  const int live = min(kTile, N - kb * kTile);
-  const float s = scale_of(__uint_as_float(vamax[bh]));
+  const float s = scale_of(__uint_as_float(amax[bh]));
   const float inv = 1.f / s;
   if (kb == 0 && threadIdx.x == 0) vscale[bh] = s;
-  uint4 vv[kChunksPerThread];
-  load_block(v, row0, live, vv);
+  const int m = threadIdx.x & 15, d0 = 8 * m;
 #pragma unroll
-  for (int i = 0; i < kChunksPerThread; ++i) {
-    const int c = i * kQThreads + threadIdx.x;
-    const int key = c >> 4, d0 = (c & 15) * 8;
-    const uint2 b = chunk_to_e4m3(vv[i], inv);  // zero chunks give zero codes
+  for (int pass = 0; pass < 2; ++pass) {
+    const int kg = pass * 16 + (threadIdx.x >> 4);  // keys 4kg .. 4kg+3 of the block
+    uint2 b[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      tile[(d0 + e) * kRow + key] = static_cast<uint8_t>(b.x >> (8 * e));
-      tile[(d0 + 4 + e) * kRow + key] = static_cast<uint8_t>(b.y >> (8 * e));
+    for (int r = 0; r < 4; ++r) {
+      const int n = kb * kTile + 4 * kg + r;
+      const uint4 q = n < N ? *reinterpret_cast<const uint4*>(
+                                  v + (static_cast<size_t>(bh) * N + n) * 128 + d0)
+                            : make_uint4(0u, 0u, 0u, 0u);
+      b[r] = chunk_to_e4m3(q, inv);  // zero chunks give zero codes
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      // byte e of each key's 8 codes (column d0 + e) into one word, key order
+      const uint32_t x0 = e < 4 ? b[0].x : b[0].y, x1 = e < 4 ? b[1].x : b[1].y;
+      const uint32_t x2 = e < 4 ? b[2].x : b[2].y, x3 = e < 4 ? b[3].x : b[3].y;
+      const uint32_t sel = static_cast<uint32_t>(e & 3) | (static_cast<uint32_t>((e & 3) + 4) << 4);
+      const uint32_t lo = __byte_perm(x0, x1, sel), hi = __byte_perm(x2, x3, sel);
+      tile[(d0 + e) * kRowWords + kg] = __byte_perm(lo, hi, 0x5410);
     }
   }
   __syncthreads();
   // thread = (d row, half): 64 keys of that row as 4 x 16 bytes
   const int dr = threadIdx.x >> 1, half = threadIdx.x & 1;
-  const uint32_t* srow = reinterpret_cast<const uint32_t*>(tile + dr * kRow) + half * 16;
+  const uint32_t* srow = tile + dr * kRowWords + half * 16;
   uint4* dst = reinterpret_cast<uint4*>(vt8 + (static_cast<size_t>(bh) * 128 + dr) * Npad +
                                         static_cast<size_t>(kb) * kTile + half * 64);
 #pragma unroll
