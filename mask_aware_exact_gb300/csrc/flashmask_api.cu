@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/flashmask.h: argument checks,
 // workspace layout, TMA descriptors and kernel launches. Nothing here
 // allocates device memory.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -101,18 +102,18 @@ fm::MaskDev mask_dev(const fm_mask* m) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // SMs of the current device (the persistent forward's grid), looked up once
-// per device.
+// per device; threads that race on the first lookup store the same value.
 int sm_count() {
   constexpr int kMaxDev = 256;
-  static int cached[kMaxDev] = {};
+  static std::atomic<int> cached[kMaxDev];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;  // a race between threads writes the same value
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
