@@ -37,20 +37,26 @@ if ROOT not in sys.path:
 METRIC = "effective TFLOP/s (unmasked FLOPs) fwd+bwd at 1 GB300; % of dense BF16 peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# Dense bf16 tensor-core rate per SM and clock: one kind::f16 MMA of
+# M = 128, N = 256, K = 16 (2*128*256*16 FLOP) per 128 cycles; measured on
+# this GPU at 128.7 cycles per instruction back to back. Times 152 SMs and the
+# sampled SM clock it is the pipe's own ceiling at that clock.
+SM_COUNT = 152
+BF16_FLOP_PER_CLK_SM = 8192
+DATASHEET_BF16_TFLOPS = 2250.0  # GB300 dense bf16, vendor figure
 
-# DRAM bytes (read + write) per launch of the attention kernels, keyed by
-# kernel, a hash of the kernel source they were measured on (a changed kernel
-# reports null) and workload. Captured with ncu on the same
-# workload at H = 8 (profiles/bwd_kernel_document_b1h8n32768d128.md,
-# profiles/fwd_kernel_document_b1h8n32768d128.md) and scaled by 4 to H = 32:
-# every head is an independent unit of identical work, so traffic grows in
-# proportion to the heads.
 # Heads per chunk of the host-buffer pipeline the end-to-end leg times (on the
 # 32K document workload, chunks of 1, 2, 4, 8, 16 heads took 9.65, 7.48, 7.76,
 # 8.70, 10.71 ms per step on GB300: copy-bound, with the first copy-in and last
 # copy-out exposed).
 E2E_CHUNK_HEADS = 2
 
+# DRAM bytes (read + write) per launch of the attention kernels, keyed by
+# kernel, a hash of the kernel source they were measured on (a changed kernel
+# reports null) and workload. Taken from one ncu capture of the kernel on the
+# same workload at H = 8 (dram__bytes_read.sum + dram__bytes_write.sum) and
+# scaled by 4 to H = 32: every head is an independent unit of identical work,
+# so traffic grows in proportion to the heads.
 NCU_TRAFFIC = {
     "bwd_main@172b1ff61d70@document_b1h32n32768d128": 4 * (405.954048e6 + 220.839424e6),
     "fwd@176d56817e16@document_b1h32n32768d128": 4 * (201.946624e6 + 49.924608e6),
@@ -150,6 +156,110 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ native arm
+KERNEL_NAMES = ["classify", "fwd", "bwd_pre", "bwd_main", "bwd_finalize"]
+
+
+def choose_peak(pk: dict, clk: dict, region_s: float) -> tuple[float, str]:
+    """The measured bf16 matmul peak that matches how the kernels ran: the
+    burst figure (a matmul timed alone, at full clock) for a region under a
+    second or one whose sampled SM clock sat at its maximum; the sustained
+    figure (seconds of back-to-back matmuls under the power cap) otherwise."""
+    burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sust = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    at_max = sm is not None and smax and sm >= 0.97 * smax
+    if region_s < 1.0 or at_max:
+        return burst, "burst"
+    return sust, "sustained"
+
+
+def clock_peak_tflops(sm_mhz) -> float | None:
+    """Dense bf16 tensor-pipe ceiling of all SMs at the sampled SM clock."""
+    if not sm_mhz:
+        return None
+    return SM_COUNT * BF16_FLOP_PER_CLK_SM * sm_mhz * 1e6 / 1e12
+
+
+class Problem:
+    """One workload's device tensors, mask, workspace and outputs."""
+
+    def __init__(self, w, dev, fm, F, W, pin=False):
+        import torch
+        self.w = w
+        B, H, N, d = w.B, w.H, w.N, w.d
+        self.scale = 1.0 / math.sqrt(d)
+        host = W.make_qkv(B, H, N, d, w.seed)
+        self.host = tuple(x.pin_memory() for x in host) if pin else None
+        self.q, self.k, self.v, self.do = (x.to(dev) for x in host)
+        self.mask = fm.DeviceMask.from_spec(w.mask, device=dev)
+        self.ws = fm.alloc_workspace(B, H, self.mask.Hm, N, d, for_bwd=True, device=dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.fl = F.effective_flops(w.mask, H, d)
+
+    def step(self, fm, stream, ev=None):
+        w, s = self.w, self.scale
+        rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
+        rec(0)
+        fm.flashmask_classify(self.mask, w.B, w.N, self.ws)
+        rec(1)
+        fm.flashmask_fwd(self.q, self.k, self.v, self.mask, self.ws, scale=s, o=self.o,
+                         lse=self.lse, ws_classified=True)
+        rec(2)
+        fm.flashmask_bwd_preprocess(self.o, self.lse, self.do, self.mask.Hm, self.ws)
+        rec(3)
+        fm.flashmask_bwd_main(self.q, self.k, self.v, self.do, self.mask, self.ws, self.dk,
+                              self.dv, scale=s)
+        rec(4)
+        fm.flashmask_bwd_finalize(self.dq, self.mask.Hm, self.ws, scale=s)
+        rec(5)
+
+
+def time_steps(prob, fm, R, stream, steps: int, warmup: int) -> dict:
+    """W untimed steps, then K timed steps between barriers and synchronises,
+    CUDA events on the launching stream around the region and around each
+    kernel of every step."""
+    import torch
+    for _ in range(warmup):
+        prob.step(fm, stream)
+    st, site = fm.flashmask_check_status(prob.ws)
+    if st != fm.FM_OK:
+        raise RuntimeError(f"device status {st} at site {site} during warm-up ({prob.w.name})")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    R.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t0.record(stream)
+    for i in range(steps):
+        prob.step(fm, stream, evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    R.barrier()
+    st, site = fm.flashmask_check_status(prob.ws)
+    if st != fm.FM_OK:
+        raise RuntimeError(f"device status {st} at site {site} in the timed region ({prob.w.name})")
+    per = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+           for j, n in enumerate(KERNEL_NAMES)}
+    return {"elapsed_s": t0.elapsed_time(t1) / 1e3, "per": per, "wall": (wall0, wall1)}
+
+
+def roofline_of(prob, per: dict, peak: float, peak_kind: str) -> dict:
+    """Roofline of the dominant kernel (the larger of the forward and the
+    backward main kernel): algorithmic FLOPs per launch (visible entries
+    only) over its mean launch time, against the chosen measured peak."""
+    dom = max(("fwd", "bwd_main"), key=lambda n: per[n])
+    dom_flops = prob.fl["bwd"] if dom == "bwd_main" else prob.fl["fwd"]
+    achieved = dom_flops / (per[dom] / 1e3) / 1e12
+    src_hash = kernel_source_hash(("bwd.cu", "ptx.cuh") if dom == "bwd_main"
+                                  else ("fwd.cu", "ptx.cuh"))
+    return {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+            "traffic": NCU_TRAFFIC.get(f"{dom}@{src_hash}@{prob.w.name}")}
+
+
 def run_native(args):
     import torch
 
@@ -173,68 +283,24 @@ def run_native(args):
         w.H = args.heads
         w.name += f"_h{args.heads}"
     B, H, N, d = w.B, w.H, w.N, w.d
-    scale = 1.0 / math.sqrt(d)
-    q_h, k_h, v_h, do_h = (x.pin_memory() for x in W.make_qkv(B, H, N, d, w.seed))
-    q, k, v, do = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
-    mask = fm.DeviceMask.from_spec(w.mask, device=dev)
-    Hm = mask.Hm
-    ws = fm.alloc_workspace(B, H, Hm, N, d, for_bwd=True, device=dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fl = F.effective_flops(w.mask, H, d)
+    prob = Problem(w, dev, fm, F, W, pin=True)
+    q_h, k_h, v_h, do_h = prob.host
+    scale, fl = prob.scale, prob.fl
     stream = torch.cuda.current_stream()
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        fm.flashmask_classify(mask, B, N, ws)
-        if ev is not None:
-            ev[1].record(stream)
-        fm.flashmask_fwd(q, k, v, mask, ws, scale=scale, o=o, lse=lse, ws_classified=True)
-        if ev is not None:
-            ev[2].record(stream)
-        fm.flashmask_bwd_preprocess(o, lse, do, Hm, ws)
-        if ev is not None:
-            ev[3].record(stream)
-        fm.flashmask_bwd_main(q, k, v, do, mask, ws, dk, dv, scale=scale)
-        if ev is not None:
-            ev[4].record(stream)
-        fm.flashmask_bwd_finalize(dq, Hm, ws, scale=scale)
-        if ev is not None:
-            ev[5].record(stream)
 
     clocks = ClockSampler(local)
     clocks.start()
-    for _ in range(args.warmup):
-        step()
-    st, site = fm.flashmask_check_status(ws)
-    if st != fm.FM_OK:
-        raise RuntimeError(f"device status {st} at site {site} during warm-up")
-
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    R.barrier()
-    torch.cuda.synchronize()
-    wall0 = time.time()
-    t0.record(stream)
-    for i in range(K):
-        step(evs[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    wall1 = time.time()
-    R.barrier()
-    clk = clocks.stop(wall0, wall1)
-    elapsed_s = t0.elapsed_time(t1) / 1e3
-    st, site = fm.flashmask_check_status(ws)
-    if st != fm.FM_OK:
-        raise RuntimeError(f"device status {st} at site {site} in the timed region")
-    names = ["classify", "fwd", "bwd_pre", "bwd_main", "bwd_finalize"]
-    per = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(names)}
-    agg = R.aggregate_throughput(fl["total"] * K, elapsed_s, dev)
+    tm = time_steps(prob, fm, R, stream, K, args.warmup)
+    clk = clocks.stop(*tm["wall"])
+    per = tm["per"]
+    agg = R.aggregate_throughput(fl["total"] * K, tm["elapsed_s"], dev)
     value = agg["throughput"] / 1e12
     ms_per_step = agg["max_elapsed_s"] / K * 1e3
+    pk, pk_src = peaks()
+    peak, peak_kind = choose_peak(pk, clk, tm["elapsed_s"])
+    cpeak = clock_peak_tflops(clk.get("sm_mhz"))
+    rl = roofline_of(prob, per, peak, f"bf16 {peak_kind} ({pk_src})")
 
     # ---------------- end to end: pinned host buffers in, results back to host,
     # through the library's host-buffer entry point (copies overlapped with the
@@ -278,12 +344,12 @@ def run_native(args):
     fp8 = None
     if d == 128:
         try:
-            ws8 = fm.alloc_fp8_workspace(B, H, Hm, N, device=dev)
-            fm.flashmask_classify(mask, B, N, ws8)
+            ws8 = fm.alloc_fp8_workspace(B, H, prob.mask.Hm, N, device=dev)
+            fm.flashmask_classify(prob.mask, B, N, ws8)
 
             def fp8_fwd():
-                fm.flashmask_fwd_fp8(q, k, v, mask, ws8, scale=scale, o=o, lse=lse,
-                                     ws_classified=True)
+                fm.flashmask_fwd_fp8(prob.q, prob.k, prob.v, prob.mask, ws8, scale=scale,
+                                     o=prob.o, lse=prob.lse, ws_classified=True)
 
             for _ in range(args.warmup):
                 fp8_fwd()
@@ -305,15 +371,37 @@ def run_native(args):
         except Exception as e:  # reported, never fatal to the headline
             fp8 = {"api": "flashmask_fwd_fp8", "error": str(e)[:200]}
 
-    pk, pk_src = peaks()
-    peak_dense = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    peak_sust = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    # dominant kernel: the backward main kernel (largest share of the step)
-    dom = max(("fwd", "bwd_main"), key=lambda n: per[n])
-    dom_flops = fl["bwd"] if dom == "bwd_main" else fl["fwd"]
-    achieved = dom_flops / (per[dom] / 1e3) / 1e12
-    src_hash = kernel_source_hash(("bwd.cu", "ptx.cuh") if dom == "bwd_main" else ("fwd.cu", "ptx.cuh"))
-    traffic = NCU_TRAFFIC.get(f"{dom}@{src_hash}@{w.name}")
+    # ---------------- the other synthetic workloads, each in the same launch
+    # configuration (rank 0 of a single-process run only; never the headline)
+    others = []
+    if world == 1 and not args.heads and not args.no_other_workloads:
+        del prob
+        torch.cuda.empty_cache()
+        for idx in range(len(W.WORKLOAD_NAMES)):
+            if idx == args.workload:
+                continue
+            try:
+                p2 = Problem(W.workload(idx), dev, fm, F, W)
+                c2 = ClockSampler(local)
+                c2.start()
+                t2 = time_steps(p2, fm, R, stream, args.other_steps, max(3, args.warmup))
+                k2 = c2.stop(*t2["wall"])
+                v2 = p2.fl["total"] * args.other_steps / t2["elapsed_s"] / 1e12
+                pk2, kind2 = choose_peak(pk, k2, t2["elapsed_s"])
+                cp2 = clock_peak_tflops(k2.get("sm_mhz"))
+                others.append({
+                    "workload": p2.w.name, "value": round(v2, 2), "unit": UNIT,
+                    "steps": args.other_steps,
+                    "ms_per_step": round(t2["elapsed_s"] / args.other_steps * 1e3, 4),
+                    "pct_of_peak": round(100 * v2 / pk2, 2),
+                    "pct_of_clock_peak": round(100 * v2 / cp2, 2) if cp2 else None,
+                    "kernels_ms": {n: round(t2["per"][n], 4) for n in KERNEL_NAMES},
+                    "roofline": roofline_of(p2, t2["per"], pk2, f"bf16 {kind2} ({pk_src})"),
+                    "clocks": k2})
+                del p2
+                torch.cuda.empty_cache()
+            except Exception as e:  # reported, never fatal to the headline
+                others.append({"workload": W.WORKLOAD_NAMES[idx], "error": str(e)[:200]})
 
     result = None
     if rank == 0:
@@ -334,21 +422,24 @@ def run_native(args):
                        "d": d, "global_batch": B * world, "seq_len": N,
                        "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                        "l2": "inputs (Q,K,V,dO = %.2f GB) larger than L2; no flush" %
-                             (4 * q.numel() * 2 / 1e9),
+                             (4 * B * H * N * d * 2 / 1e9),
                        "nnz_per_replica": fl["nnz"],
                        "flops_per_step_per_replica": fl["total"]},
-            "pct_of_peak": round(100 * value / world / peak_dense, 2),
-            "peak_bf16_tflops": peak_dense,
+            "pct_of_peak": round(100 * value / world / peak, 2),
+            "pct_of_peak_note": f"fraction of the measured cuBLAS bf16 matmul throughput "
+                                f"({peak_kind}, {pk_src}); the same peak as roofline.peak",
+            "pct_of_clock_peak": round(100 * value / world / cpeak, 2) if cpeak else None,
+            "pct_of_clock_peak_note": f"fraction of the dense bf16 tensor-pipe rate at the "
+                                      f"sampled SM clock ({SM_COUNT} SMs x "
+                                      f"{BF16_FLOP_PER_CLK_SM} FLOP/clk x sm_mhz)",
+            "pct_of_datasheet": round(100 * value / world / DATASHEET_BF16_TFLOPS, 2),
+            "peak_bf16_tflops": peak,
             "peak_source": pk_src,
-            "kernels_ms": {n: round(per[n], 4) for n in names},
+            "kernels_ms": {n: round(per[n], 4) for n in KERNEL_NAMES},
             "fwd_tflops": round(fl["fwd"] / (per["fwd"] / 1e3) / 1e12, 1),
             "bwd_tflops": round(fl["bwd"] / ((per["bwd_pre"] + per["bwd_main"] + per["bwd_finalize"])
                                              / 1e3) / 1e12, 1),
-            "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
-                         "peak": peak_sust, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak_sust, 4),
-                         "peak_kind": f"bf16 sustained ({pk_src})",
-                         "traffic": traffic},
+            "roofline": rl,
             "e2e": {"value": round(e2e_agg["throughput"] / 1e12, 2), "unit": UNIT,
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "api": "flashmask_fwd_bwd_host", "chunk_heads": chunk,
@@ -358,6 +449,8 @@ def run_native(args):
         }
         if fp8 is not None:
             result["fp8_forward"] = fp8
+        if others:
+            result["other_workloads"] = others
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(w, args.oracle_seconds)
     R.finalize()
@@ -450,6 +543,9 @@ def main():
     ap.add_argument("--workload", type=int, default=2, help="synthetic workload index 0..4")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-seconds", type=float, default=12.0)
+    ap.add_argument("--other-steps", type=int, default=20,
+                    help="timed steps of each other workload (reported in other_workloads)")
+    ap.add_argument("--no-other-workloads", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
                     help="override H (profiling captures on a smaller case only; not a bench line)")
     args = ap.parse_args()

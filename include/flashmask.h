@@ -35,6 +35,15 @@
  * fp32 scratch and a device status word. One workspace must not be used by two
  * calls that may run at the same time.
  *
+ * The status word (the first 16 bytes of the workspace) must be zero before
+ * the workspace is first passed to a call that launches kernels: allocate the
+ * workspace zeroed (cudaMemset, torch.zeros) or call flashmask_check_status()
+ * on it once, which reads the word and clears it. The calls themselves do not
+ * clear it (a failure recorded by one call stays visible until it is checked),
+ * and a kernel that finds it nonzero gives up every wait that is not already
+ * satisfied, leaving its outputs undefined; flashmask_check_status() then
+ * reports FM_ERR_TIMEOUT.
+ *
  * Streams and errors: every call validates its arguments on the host and
  * returns an error WITHOUT launching anything if they are bad. Otherwise it
  * enqueues kernels on `stream` (a cudaStream_t, NULL for the legacy default
@@ -85,7 +94,8 @@ typedef struct {
 /* Byte offsets of the workspace regions (from the workspace base), for callers
  * that want to read the classification. Regions marked [bwd] exist only when
  * the workspace was sized with for_bwd != 0 (otherwise their offsets are 0).
- *   status    int32[4]                   device status word (0 = OK), detail, and the
+ *   status    int32[4]                   device status word (0 = OK; must be zero
+ *                                        before first use, see above), detail, and the
  *                                        forward's work-item counter (reset by each call)
  *   minmax    int32  [B,Hm,Tc,8]         per key block: min/max of LTS, LTE, UTS, UTE
  *   labels    uint8  [B,Hm,Tr,Tc]        tile label, query-block major

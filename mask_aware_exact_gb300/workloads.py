@@ -185,6 +185,45 @@ def block_causal_bounds(B: int, Hm: int, N: int, block: int) -> MaskSpec:
                     bc(ute), {"block": block})
 
 
+def block_sparse_runs(N: int, block: int, seed: int, global_blocks: int = 1):
+    """Seeded block-sparse pattern: for every key block c (``block`` keys) a run
+    [a_c, b_c] of query blocks that see it, drawn from
+    ``numpy.random.default_rng(seed)`` with a_c uniform in [0, c] and b_c
+    uniform in [c, nb - 1] (so the diagonal block stays visible); the first
+    ``global_blocks`` key blocks are seen by every query block (a = 0,
+    b = nb - 1). Returns int lists (a, b) of length nb = ceil(N / block)."""
+    rng = np.random.default_rng(seed)
+    nb = (N + block - 1) // block
+    a, b = [], []
+    for c in range(nb):
+        if c < global_blocks:
+            a.append(0)
+            b.append(nb - 1)
+        else:
+            a.append(int(rng.integers(0, c + 1)))
+            b.append(int(rng.integers(c, nb)))
+    return a, b
+
+
+def block_sparse_bounds(B: int, Hm: int, N: int, block: int, seed: int,
+                        global_blocks: int = 1) -> MaskSpec:
+    """Block-sparse mask in which every key block is seen by one contiguous run
+    of query blocks (``block_sparse_runs``), causal=False: a key in block c
+    masks the rows before its run (upper interval [0, a_c * block)) and the
+    rows after it (lower interval [(b_c + 1) * block, N)). Patterns in which a
+    key block is seen by two separate runs need more than two intervals per
+    column and are not representable in this encoding."""
+    a, b = block_sparse_runs(N, block, seed, global_blocks)
+    c = np.arange(N) // block
+    ute = (np.asarray(a, np.int64)[c] * block).astype(np.int32)
+    lts = np.minimum((np.asarray(b, np.int64)[c] + 1) * block, N).astype(np.int32)
+    bc = lambda x: np.broadcast_to(x, (B, Hm, N)).copy()
+    return MaskSpec("block_sparse", False, bc(lts), bc(np.full(N, N, np.int32)),
+                    bc(np.zeros(N, np.int32)), bc(ute),
+                    {"block": block, "seed": seed, "global_blocks": global_blocks,
+                     "runs": (a, b)})
+
+
 def stack_heads(specs: list[MaskSpec]) -> MaskSpec:
     """One mask per head (Hm = len(specs)): the specs' [B, 1, N] vectors side by
     side. All must share B, N and the causal flag; a spec without an upper

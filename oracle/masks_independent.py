@@ -47,6 +47,17 @@ def block_causal(N: int, block: int, rows=None) -> np.ndarray:
     return (j // block) <= (i // block)
 
 
+def block_sparse(N: int, block: int, runs, rows=None) -> np.ndarray:
+    """Block-level visibility expanded to elements: query block r sees key
+    block c iff a_c <= r <= b_c, with runs = (a, b) listed per key block."""
+    a, b = (np.asarray(x) for x in runs)
+    nb = len(a)
+    r_blk = np.arange(nb)[:, None]
+    vis_blocks = (a[None, :] <= r_blk) & (r_blk <= b[None, :])  # [query block, key block]
+    dense = np.kron(vis_blocks, np.ones((block, block), bool))[:N, :N]
+    return dense if rows is None else dense[np.asarray(rows)]
+
+
 def share_question(q_len: int, answers, rows=None) -> np.ndarray:
     """Question rows see the question causally; an answer row sees the whole
     question before it and its own answer causally, never another answer."""

@@ -151,12 +151,25 @@ def sampled_compare(w, out, q, k, v, do, heads, row_blocks, key_blocks):
         check_grad("V", to_np(out["dv"][b, h])[keys], dv_ref[keys], f"{w.name} head {(b, h)}")
 
 
+def _every(step, n, extra=()):
+    return sorted(set(range(0, n, step)) | set(extra))
+
+
 SAMPLES = {
-    # workload index: (heads, query blocks, key blocks)
-    1: ([(0, 0), (3, 15)], [0, 31, 63], [0, 40, 63]),
-    2: ([(0, 0), (0, 31)], [0, 55, 56, 200, 255], [3, 60, 180, 255]),
-    3: ([(0, 0), (1, 31)], [0, 31, 40, 90, 127], [5, 33, 64, 120]),
-    4: ([(0, 0), (0, 7)], [0, 15, 16, 17, 500, 1023], [16, 17, 400, 1023]),
+    # workload index: (heads, query blocks, key blocks). Heads: the first and
+    # the last of the head-major work order (the persistent forward and the
+    # backward visit heads in order, longest blocks first within a head, so
+    # these are the first and last heads the CTAs take); query blocks: every
+    # 8th plus the blocks at document, question, window and prefix edges; key
+    # blocks spread over the sequence.
+    1: ([(0, 0), (1, 7), (3, 15)], _every(8, 64, [31, 63]), [0, 9, 20, 31, 40, 52, 63]),
+    2: ([(0, 0), (0, 31)], _every(8, 256, [55, 56, 97, 255]),
+        [3, 33, 60, 100, 140, 180, 220, 255]),
+    3: ([(0, 0), (1, 31)], _every(8, 128, [31, 32, 81, 93, 114, 127]),
+        [5, 33, 48, 64, 81, 100, 120, 127]),
+    # at 128K every sampled row costs the oracle a 131072-key softmax: the
+    # prefix edge (blocks 15 | 16), the first full window (31, 32) and the end
+    4: ([(0, 0), (0, 7)], [0, 15, 16, 17, 31, 32, 500, 1022, 1023], [16, 17, 400, 1023]),
 }
 
 
@@ -208,11 +221,17 @@ def test_ragged_sequence_lengths(N, d, kind):
 @pytest.mark.parametrize("kind,N,d", [("bidirectional_document", 640, 128),
                                       ("bidirectional_document", 300, 64),
                                       ("block_causal", 640, 64), ("block_causal", 500, 128),
-                                      ("per_head", 384, 128)])
+                                      ("per_head", 384, 128), ("block_sparse", 1024, 128),
+                                      ("block_sparse", 700, 64), ("block_sparse", 896, 128)])
 def test_more_mask_families(kind, N, d):
     fm = need_gpu()
     B = 2
-    if kind == "bidirectional_document":
+    if kind == "block_sparse":
+        # seeded runs of query blocks per key block plus a global first block;
+        # block 64 (N = 700) and 96 (N = 896) make tiles with mixed columns
+        block = {1024: 128, 700: 64, 896: 96}[N]
+        spec, H = W.block_sparse_bounds(B, 1, N, block, seed=N), 2
+    elif kind == "bidirectional_document":
         lengths = [N // 3, N // 4, N - N // 3 - N // 4]
         spec, H = W.bidirectional_document_bounds(B, 1, lengths), 2
     elif kind == "block_causal":

@@ -37,3 +37,24 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     out = run_path(fm, q, k, v, do, w.mask)
     o_ref, lse_ref = A.forward(q, k, v, w.mask, 1 / math.sqrt(w.d))
     check_forward(to_np(out["o"]), to_np(out["lse"]), o_ref, lse_ref, "after self-test")
+
+
+def test_uninitialised_status_word_is_reported_and_cleared():
+    # A workspace that was not allocated zeroed: the documented way to make it
+    # usable is one flashmask_check_status(), which reports what the status
+    # word held (as a timeout with that detail) and clears it. No kernel runs
+    # on the poisoned word.
+    fm = need_gpu()
+    w = W.workload(0)
+    ws = torch.empty(fm.flashmask_workspace_bytes(w.B, w.H, 1, w.N, w.d, True),
+                     dtype=torch.uint8, device="cuda")
+    ws[:16].copy_(torch.tensor(np.array([0x7f, 0x12345, 0, 0], np.int32).view(np.uint8)))
+    st, site = fm.flashmask_check_status(ws)
+    assert (st, site) == (fm.FM_ERR_TIMEOUT, 0x12345)
+    assert fm.flashmask_check_status(ws) == (fm.FM_OK, 0)
+    q, k, v, do = W.make_qkv(w.B, w.H, w.N, w.d, w.seed)
+    mask = fm.DeviceMask.from_spec(w.mask)
+    o, lse = fm.flashmask_fwd(q.cuda(), k.cuda(), v.cuda(), mask, ws)
+    assert fm.flashmask_check_status(ws) == (fm.FM_OK, 0)
+    o_ref, lse_ref = A.forward(q, k, v, w.mask, 1 / math.sqrt(w.d))
+    check_forward(to_np(o), to_np(lse), o_ref, lse_ref, "after clearing")

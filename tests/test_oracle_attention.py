@@ -175,3 +175,55 @@ def test_mask_heads_broadcast():
         o, _ = A.forward_head(q[0, h], k[0, h], v[0, h], src.lts[0, 0], src.lte[0, 0], None, None,
                               True, 0.3)
         np.testing.assert_allclose(O[0, h], o, atol=0)
+
+
+def test_batched_wrappers_vs_torch_autograd_per_head_masks():
+    # The [B, H] wrappers against torch fp64 SDPA + autograd on the whole
+    # batch at once, with a different dense mask for each (batch, mask head)
+    # written straight from the family definitions (not from boundary
+    # vectors). B = 2, H = 4, Hm = 2: heads 0, 1 read mask head 0 and heads
+    # 2, 3 read mask head 1, so a wrong head -> mask-head mapping, a swapped
+    # batch, or a permuted (dQ, dK, dV) return order fails here.
+    from oracle import masks_independent as MI
+    B, H, N, d = 2, 4, 40, 8
+    docs = [[12, 28], [25, 15]]
+    families = {  # (b, hm) -> (bounds spec [1, 1, N], dense visibility)
+        (0, 0): (W.document_bounds(1, 1, docs[0]), MI.causal_document(docs[0])),
+        (0, 1): (W.causal_bounds(1, 1, N), MI.causal(N)),
+        (1, 0): (W.share_question_bounds(1, 1, 10, [18, 12]), MI.share_question(10, [18, 12])),
+        (1, 1): (W.document_bounds(1, 1, docs[1]), MI.causal_document(docs[1])),
+    }
+    cat = lambda name: np.concatenate(
+        [np.concatenate([getattr(families[(b, hm)][0], name) for hm in range(2)], 1)
+         for b in range(B)], 0)
+    spec = W.MaskSpec("per_batch_head", True, cat("lts"), cat("lte"), None, None)
+    dense = np.zeros((B, H, N, N), bool)
+    for b in range(B):
+        for h in range(H):
+            dense[b, h] = families[(b, 0 if h < 2 else 1)][1]
+    q, k, v, do = (rand((B, H, N, d), 70 + i) for i in range(4))
+    scale = 0.3
+    O, LSE = A.forward(q, k, v, spec, scale)
+    dq, dk, dv = A.backward(q, k, v, do, spec, scale)
+    t = lambda x: torch.tensor(x, dtype=torch.float64, requires_grad=True)
+    tq, tk, tv = t(q), t(k), t(v)
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv,
+                                                         attn_mask=torch.tensor(dense),
+                                                         scale=scale)
+    (o * torch.tensor(do)).sum().backward()
+    np.testing.assert_allclose(O, o.detach().numpy(), atol=1e-12)
+    S = np.where(dense, scale * np.einsum("bhid,bhjd->bhij", q, k), -np.inf)
+    np.testing.assert_allclose(LSE, logsumexp(S, axis=-1), atol=1e-12)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-11)
+
+
+def test_batched_wrapper_heads_subset_leaves_others_unset():
+    # only the requested heads are computed; the rest stay NaN
+    B, H, N, d = 1, 3, 16, 4
+    spec = W.causal_bounds(B, 1, N)
+    q, k, v, do = (rand((B, H, N, d), 80 + i) for i in range(4))
+    dq, dk, dv = A.backward(q, k, v, do, spec, 0.5, heads=[(0, 1)])
+    for g in (dq, dk, dv):
+        assert np.isnan(g[0, 0]).all() and np.isnan(g[0, 2]).all() and np.isfinite(g[0, 1]).all()

@@ -130,3 +130,18 @@ def test_stack_heads_decodes_each_head():
     rows = np.arange(N)
     assert np.array_equal(decoded(spec, rows, hm=0), MI.causal_document([120, 80], rows))
     assert np.array_equal(decoded(spec, rows, hm=1), MI.causal(N, rows))
+
+
+@pytest.mark.parametrize("N,block,seed", [(640, 64, 0), (1024, 128, 1), (700, 96, 2),
+                                          (300, 128, 3)])
+def test_block_sparse(N, block, seed):
+    spec = W.block_sparse_bounds(1, 1, N, block, seed)
+    runs = spec.params["runs"]
+    compare_blocked(spec, lambda r: MI.block_sparse(N, block, runs, r), block=128)
+    # the runs themselves: each contains its diagonal block; block 0 is global
+    a, b = runs
+    assert a[0] == 0 and b[0] == len(a) - 1
+    assert all(a[c] <= c <= b[c] for c in range(len(a)))
+    # the pattern is not a plain causal / banded one: some key block is hidden
+    # from some query block above and below its run
+    assert any(x > 0 for x in a[1:]) and any(y < len(a) - 1 for y in b[1:])

@@ -81,3 +81,26 @@ def test_minmax_hand_worked():
     lte = np.full(N, 7)
     mm = TL.key_block_minmax(N, lts, lte, None, None)
     assert mm.tolist() == [[128, 255, 7, 7, 0, 0, 0, 0], [0, 127, 7, 7, 0, 0, 0, 0]]
+
+
+def test_minmax_hand_worked_upper_vectors():
+    # distinct, non-trivial values in all four vectors so that every one of
+    # the eight columns (min/max of LTS, LTE, UTS, UTE) has its own hand value
+    N = 256
+    j = np.arange(N)
+    lts = 2 * j            # block 0: 0..254,   block 1: 256..510
+    lte = 1000 - j         # block 0: 873..1000, block 1: 745..872
+    uts = j                # block 0: 0..127,   block 1: 128..255
+    ute = N - j            # block 0: 129..256, block 1: 1..128
+    mm = TL.key_block_minmax(N, lts, lte, uts, ute)
+    assert mm.tolist() == [[0, 254, 873, 1000, 0, 127, 129, 256],
+                           [256, 510, 745, 872, 128, 255, 1, 128]]
+
+
+def test_minmax_short_last_block():
+    # N = 200: the second key block holds keys 128..199 only
+    N = 200
+    j = np.arange(N)
+    mm = TL.key_block_minmax(N, j + 5, 3 * j, N - j, np.full(N, 9))
+    assert mm.tolist() == [[5, 132, 0, 381, 73, 200, 9, 9],
+                           [133, 204, 384, 597, 1, 72, 9, 9]]

@@ -1,6 +1,7 @@
 """The allocation-free forward (flashmask_fwd_noalloc) against the workspace
 forward (flashmask_fwd): same inputs, outputs equal within the parity
-tolerances, on two calls in a row that reuse the library's fixed scratch.
+tolerances, on two calls in a row that reuse the library's fixed scratch; the
+first call is also compared with the fp64 oracle directly.
 
 The file name sorts last so that the GPU test also runs after every other test
 of the suite, when the scratch and the CUDA context have seen other work."""
@@ -14,7 +15,7 @@ from mask_aware_exact_gb300 import build as BLD
 from mask_aware_exact_gb300 import flashmask as fm
 from mask_aware_exact_gb300 import workloads as W
 
-from gpu_common import TOL_LSE, TOL_O, need_gpu, to_np
+from gpu_common import TOL_LSE, TOL_O, check_forward, need_gpu, to_np
 
 FAKE = 1 << 20  # a 256-aligned non-null address; validation fails before it is used
 
@@ -100,18 +101,23 @@ def make_case(kind, B, H, N, d, seed):
     else:
         spec = W.random_bounds(B, 2, N, causal=True, seed=40 + seed, upper=True)
     q, k, v, _ = W.make_qkv(B, H, N, d, seed)
-    return spec, q.cuda(), k.cuda(), v.cuda()
+    return spec, q, k, v
 
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_forward_twice():
     need_gpu()
     lib = fm.load()
+    from oracle import attention as A
     for case in CASES:
-        spec, q, k, v = make_case(*case)
+        spec, q_h, k_h, v_h = make_case(*case)
+        q, k, v = q_h.cuda(), k_h.cuda(), v_h.cuda()
         mask = fm.DeviceMask.from_spec(spec)
         ref = workspace_forward(q, k, v, mask)
         first = noalloc_forward(lib, q, k, v, mask)
         second = noalloc_forward(lib, q, k, v, mask)
         assert_close(first, ref, f"{case} first call")
         assert_close(second, ref, f"{case} second call")
+        # and the first call straight against the fp64 oracle
+        o_ref, lse_ref = A.forward(q_h, k_h, v_h, spec, q.shape[-1] ** -0.5)
+        check_forward(first[0], first[1], o_ref, lse_ref, f"{case} vs oracle")
