@@ -237,12 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&mdo);
       mbar_arrive_expect_tx(bar.kv_full(), 2 * L::kTileBytes);
       for (int ch = 0; ch < L::kChunks; ++ch) {
-        tma_load_2d(sK + ch * 16384, &mk, ch * 64, k_row0, bar.kv_full());
-        tma_load_2d(sV + ch * 16384, &mv, ch * 64, k_row0, bar.kv_full());
+        tma_load_3d(sK + ch * 16384, &mk, ch * 64, kb * kTile, bh, bar.kv_full());
+        tma_load_3d(sV + ch * 16384, &mv, ch * 64, kb * kTile, bh, bar.kv_full());
       }
       for (int t = 0; t < ntiles; ++t) {
         const int st = t & 1;
-        const int q_row = head_row0 + (list[t] >> 2) * kTile;
+        const int q_row = (list[t] >> 2) * kTile;  // first row of the query block in its head
         // lse2 and D live in the padded [B*H, Npad] workspace arrays
         const size_t prow = static_cast<size_t>(bh) * p.Npad + (list[t] >> 2) * kTile;
         // Q and lse2 of stage st (freed once the dQ boxes staged in the Q
@@ -253,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(bar.q_full(st), L::kTileBytes + kTile * 4);
         for (int ch = 0; ch < L::kChunks; ++ch)
-          tma_load_2d(sQ + st * L::kTileBytes + ch * 16384, &mq, ch * 64, q_row, bar.q_full(st));
+          tma_load_3d(sQ + st * L::kTileBytes + ch * 16384, &mq, ch * 64, q_row, bh,
+                      bar.q_full(st));
         bulk_load(smem_u32(lse_s + st * kTile), p.lse2 + prow, kTile * 4, bar.q_full(st));
         // ... then dO and D (freed when the boxes staged in the dO buffer have
         // been read), so that S and P of a tile can start before its dO lands
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(bar.do_full(st), L::kTileBytes + kTile * 4);
         for (int ch = 0; ch < L::kChunks; ++ch)
-          tma_load_2d(sDO + st * L::kTileBytes + ch * 16384, &mdo, ch * 64, q_row,
+          tma_load_3d(sDO + st * L::kTileBytes + ch * 16384, &mdo, ch * 64, q_row, bh,
                       bar.do_full(st));
         bulk_load(smem_u32(delta_s + st * kTile), p.delta + prow, kTile * 4, bar.do_full(st));
       }

@@ -22,6 +22,9 @@ int padded(int N) { return blocks_of(N) * kTile; }
 
 bool shape_ok(int B, int H, int Hm, int N, int d) {
   if (B <= 0 || H <= 0 || Hm <= 0 || N <= 0) return false;
+  // the classification keeps per-query-block arrays of one key block in shared
+  // memory (2 * 4 * (Tr + 1) bytes)
+  if (N > FM_MAX_SEQLEN) return false;
   if (d != 64 && d != 128) return false;
   if (H % Hm != 0) return false;
   const long long rows = static_cast<long long>(B) * H * padded(N);
@@ -55,6 +58,13 @@ fm_ws_layout make_layout(int B, int H, int Hm, int N, int d, int for_bwd) {
   off = align_up(off + BHm * Tc * Tr * 4, 256);
   L.col_order = off;
   off = align_up(off + BHm * Tc * 4, 256);
+  const size_t Tp = (Tr + 1) / 2;
+  L.pair_count = off;
+  off = align_up(off + BHm * Tp * 4, 256);
+  L.pair_list = off;
+  off = align_up(off + BHm * Tp * Tc * 4, 256);
+  L.pair_order = off;
+  off = align_up(off + BHm * Tp * 4, 256);
   if (for_bwd) {
     L.lse2 = off;
     off = align_up(off + BHN * 4, 256);
@@ -79,6 +89,9 @@ fm::ClassifyTables tables(const fm_ws_layout& L, void* ws) {
   t.col_count = reinterpret_cast<int32_t*>(w + L.col_count);
   t.col_list = reinterpret_cast<int32_t*>(w + L.col_list);
   t.col_order = reinterpret_cast<int32_t*>(w + L.col_order);
+  t.pair_count = reinterpret_cast<int32_t*>(w + L.pair_count);
+  t.pair_list = reinterpret_cast<int32_t*>(w + L.pair_list);
+  t.pair_order = reinterpret_cast<int32_t*>(w + L.pair_order);
   return t;
 }
 
@@ -151,18 +164,23 @@ bool make_map_f32(CUtensorMap* m, const void* base, long long rows, int d) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor map over a [rows, d] bf16 matrix with 128-row x 64-column boxes and
-// 128-byte swizzle (the layout the tcgen05 descriptors expect).
-bool make_map(CUtensorMap* m, const void* base, long long rows, int d) {
+// Tensor map over [heads, N, cols] (elements of `esize` bytes: bf16 or e4m3)
+// with boxes of one head, 128 rows and 128 bytes per row, 128-byte swizzle.
+// Each head is its own 2-D slab: a box that runs past row N of a head reads
+// zeros, never the next head's rows.
+bool make_map3(CUtensorMap* m, const void* base, long long heads, int N, int cols, int esize) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * esize,
+                           static_cast<cuuint64_t>(N) * cols * esize};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Tensor map over a [rows, cols] byte matrix (e4m3) with 128 x 128-byte boxes
@@ -257,9 +275,10 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
   const fm_ws_layout L = make_layout(B, H, mask->Hm, N, d, 0);
   const fm_status ws_st = check_ws(ws, ws_bytes, L);
   if (ws_st != FM_OK) return ws_st;
-  const long long rows = static_cast<long long>(B) * H * N;
+  const long long heads = static_cast<long long>(B) * H;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, rows, d) || !make_map(&mk, k, rows, d) || !make_map(&mv, v, rows, d))
+  if (!make_map3(&mq, q, heads, N, d, 2) || !make_map3(&mk, k, heads, N, d, 2) ||
+      !make_map3(&mv, v, heads, N, d, 2))
     return FM_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const fm::ClassifyTables t = tables(L, ws);
@@ -275,9 +294,10 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
   p.Tc = blocks_of(N);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.qscale = p.kscale = p.vscale = nullptr;
-  p.row_count = t.row_count;
-  p.row_list = t.row_list;
-  p.row_order = t.row_order;
+  p.Tp = (p.Tr + 1) / 2;
+  p.pair_count = t.pair_count;
+  p.pair_list = t.pair_list;
+  p.pair_order = t.pair_order;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.status = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.status);
@@ -329,9 +349,8 @@ fm_status flashmask_fwd_fp8(const void* q, const void* k, const void* v, const f
   f.vscale = reinterpret_cast<float*>(w + F.vscale);
   f.vamax = reinterpret_cast<unsigned int*>(w + F.vamax);
   const int BH = B * H;
-  const long long rows = static_cast<long long>(BH) * N;
   CUtensorMap mq, mk, mv;
-  if (!make_map_u8(&mq, f.q8, rows, 128) || !make_map_u8(&mk, f.k8, rows, 128) ||
+  if (!make_map3(&mq, f.q8, BH, N, 128, 1) || !make_map3(&mk, f.k8, BH, N, 128, 1) ||
       !make_map_u8(&mv, f.vt8, static_cast<long long>(BH) * 128, padded(N)))
     return FM_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -353,9 +372,10 @@ fm_status flashmask_fwd_fp8(const void* q, const void* k, const void* v, const f
   p.qscale = f.qscale;
   p.kscale = f.kscale;
   p.vscale = f.vscale;
-  p.row_count = t.row_count;
-  p.row_list = t.row_list;
-  p.row_order = t.row_order;
+  p.Tp = (p.Tr + 1) / 2;
+  p.pair_count = t.pair_count;
+  p.pair_list = t.pair_list;
+  p.pair_order = t.pair_order;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.status = reinterpret_cast<int32_t*>(w + F.base.status);
@@ -396,13 +416,14 @@ fm_status flashmask_bwd_main(const void* q, const void* k, const void* v, const 
   const fm_ws_layout L = make_layout(B, H, mask->Hm, N, d, 1);
   const fm_status ws_st = check_ws(ws, ws_bytes, L);
   if (ws_st != FM_OK) return ws_st;
-  const long long rows = static_cast<long long>(B) * H * N;
-  const long long rows_pad = static_cast<long long>(B) * H * padded(N);
+  const long long heads = static_cast<long long>(B) * H;
+  const long long rows_pad = heads * padded(N);
   char* w = static_cast<char*>(ws);
   float* dq_accum = reinterpret_cast<float*>(w + L.dq_accum);
   CUtensorMap mq, mk, mv, mdo, mdq;
-  if (!make_map(&mq, q, rows, d) || !make_map(&mk, k, rows, d) || !make_map(&mv, v, rows, d) ||
-      !make_map(&mdo, dout, rows, d) || !make_map_f32(&mdq, dq_accum, rows_pad, d))
+  if (!make_map3(&mq, q, heads, N, d, 2) || !make_map3(&mk, k, heads, N, d, 2) ||
+      !make_map3(&mv, v, heads, N, d, 2) || !make_map3(&mdo, dout, heads, N, d, 2) ||
+      !make_map_f32(&mdq, dq_accum, rows_pad, d))
     return FM_ERR_CUDA;
   const fm::ClassifyTables t = tables(L, ws);
   fm::BwdParams p;
