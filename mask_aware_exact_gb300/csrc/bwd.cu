@@ -114,12 +114,6 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 __device__ __forceinline__ void drain_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
 
 // ---------------------------------------------------------------- preprocess
 // One padded row (bh, n) per D/8 threads, n < Npad: rows n >= N (the short last

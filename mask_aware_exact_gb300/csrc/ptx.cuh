@@ -384,6 +384,13 @@ __device__ __forceinline__ uint32_t warp_transpose_bits(uint32_t x) {
   return x;
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
 // Byte offset of the 16-byte chunk `c16` of row `row` inside a 128-byte-swizzled
 // tile whose rows are 128 bytes long (the layout described above).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t c16) {
