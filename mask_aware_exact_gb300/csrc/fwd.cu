@@ -7,39 +7,41 @@
 //
 // A work item is one head's pair of adjacent query blocks (r0, r1) = (2p,
 // 2p + 1). Both tiles walk the merged list of key blocks that are non-FULL for
-// either of them; each K and V block is loaded once and serves both. Every
-// tile t has its own MMA-issuing warp and softmax warpgroup:
+// either of them; each K and V block is loaded once and serves both. Each tile
+// t has one chain through the tensor cores and TMEM,
 //
-//     S_t(j) = Q_t K_j^T    (TMEM)          O_t += P_t(j) V_j    (P_t from shared memory)
+//     S_t = Q_t K_j^T -> softmax_t (P_t over S_t) -> O_t += P_t V_j -> S_t of the next block,
 //
-// The softmax loads S_t(j) into registers and at once releases its TMEM
-// columns, so S_t(j+1) is computed on the tensor cores while the softmax of
-// step j runs; P_t(j) goes to a shared-memory buffer of its own, which the
-// next step overwrites only after O_t += P_t(j) V_j has completed. Neither
-// tile's chain waits for a P V product before its next S product. A tile skips
-// the key blocks that are FULL for it.
+// and one softmax warpgroup. A single thread issues both tiles' products in the
+// order S_0(j), O_1 += P_1 V (tile 1's previous step), S_1(j), O_0 += P_0 V
+// (step j), so that while one tile's softmax works the tensor pipe holds the
+// other tile's products and the two softmax warpgroups take turns. P stays in
+// TMEM (the A operand of P V), which keeps the shared-memory traffic of a step
+// to the Q K^T operands and V: with both operands of an M = N = 128 product in
+// shared memory the tensor cores' shared-memory reads (about 128 bytes per
+// clock) are already the limit. A tile skips the key blocks that are FULL for
+// it.
 //
 // Persistent CTAs (one per SM) take items from a work counter in the
 // workspace, head-major (a head's K and V stay in L2 while its pairs run) and
-// longest pair first within a head. Warp roles (512 threads):
+// longest pair first within a head. Warp roles (384 threads):
 //   warps 0-3   softmax of tile 0: thread = query row = TMEM lane, the whole
 //               128-key row of S in registers: element mask on PARTIAL tiles,
 //               row maximum, exponentials (log2 domain), row sum, P as bf16 (or
-//               e4m3) into shared memory. O_t is rescaled only when the maximum
-//               grows by more than 2^8 (lazy rescaling, exact after the final
-//               division). Epilogue: O_t / l, LSE.
+//               e4m3) over S_t. O_t is rescaled only when the maximum grows by
+//               more than 2^8 (lazy rescaling, exact after the final division).
+//               Epilogue: O_t / l, LSE.
 //   warps 4-7   softmax of tile 1.
 //   warp 8      work scheduler; TMA producer of Q_0, Q_1 (once per item) and
 //               of the K ring.
-//   warp 9, 11  S issuers of tiles 0 and 1 (one thread each).
+//   warp 9      MMA issuer of both tiles (one thread).
 //   warp 10     TMA producer of the V ring.
-//   warp 12, 13 P V issuers of tiles 0 and 1 (one thread each). S and P V of a
-//               tile come from different threads, so that neither waits
-//               behind the other's ring slots.
-//   warp 14, 15 idle (they complete the register-split warpgroup).
+//   warp 11     idle (completes the register-split warpgroup).
 //
-// TMEM columns (512): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
-// O_1 [384,384+d).
+// TMEM columns (512): S_0/P_0 [0,128), S_1/P_1 [128,256), O_0 [256,256+d),
+// O_1 [384,384+d). S_t of the next block is issued only after O_t += P_t V
+// has completed (the product reads P_t from S_t's columns), so by the time the
+// softmax sees S_t complete, O_t is quiescent and may be rescaled in place.
 #include "internal.h"
 #include "ptx.cuh"
 #include "ptx_fp8.cuh"
@@ -49,22 +51,22 @@ namespace fm {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // FP8: P is stored as e4m3(p * kFp8PScale). With the running maximum lagging
 // by at most kRescaleThresholdFp8 (log2 units), p < 2^threshold and
 // p * kFp8PScale stays below 448, the largest finite e4m3 value.
 constexpr float kRescaleThresholdFp8 = 4.0f;
 constexpr float kFp8PScale = 28.0f;
-// Roles that read each published work item: the four MMA-issuing warps, the V
-// producer and the first warp of each softmax warpgroup (which shares it with
-// the other three through shared memory).
-constexpr int kSchedReaders = 7;
+// Roles that read each published work item: the MMA warp, the V producer and
+// the first warp of each softmax warpgroup (which shares it with the other
+// three through shared memory).
+constexpr int kSchedReaders = 4;
 // Per-thread register limits after the split (setmaxnreg): softmax warpgroups,
-// producer / MMA warpgroups. Their sum over the 512 threads must not exceed the
+// producer / MMA warpgroup. Their sum over the 384 threads must not exceed the
 // pool the CTA is launched with (threads x registers of the compiled kernel).
-constexpr int kRegsSoftmax = 200, kRegsOther = 56;
-constexpr int kRegPool = 256 * kRegsSoftmax + 256 * kRegsOther;
+constexpr int kRegsSoftmax = 208, kRegsOther = 88;
+constexpr int kRegPool = 256 * kRegsSoftmax + 128 * kRegsOther;
 
 __device__ __forceinline__ uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * static_cast<uint32_t>(t); }
@@ -74,24 +76,20 @@ struct FwdLayout {
   static constexpr int kTileBytes = kTile * D * (kFp8 ? 1 : 2);  // one 128 x d tile
   static constexpr int kChunks = kFp8 ? 1 : D / 64;  // 128-byte-wide TMA boxes per tile
   static constexpr int kChunk = 16384;              // 128 rows x 128 bytes
-  static constexpr int kPBytes = kTile * kTile * (kFp8 ? 1 : 2);  // P: 128 rows x 128 keys
-  // d = 128, bf16: 64 KB of Q and 64 KB of P leave room for two K tiles and
-  // one V tile (P V is off the softmax's critical path, so one V slot keeps up)
-  static constexpr int kKSlots = kTileBytes >= 32768 ? 2 : 3;
-  static constexpr int kVSlots = kTileBytes >= 32768 ? 1 : 3;
+  static constexpr int kKSlots = kTileBytes >= 32768 ? 3 : 4;
+  static constexpr int kVSlots = kTileBytes >= 32768 ? 2 : 4;
   static constexpr int kQ = 0;                            // Q_0, Q_1
-  static constexpr int kP = kQ + 2 * kTileBytes;          // P_0, P_1
-  static constexpr int kK = kP + 2 * kPBytes;             // kKSlots x kTileBytes
+  static constexpr int kK = kQ + 2 * kTileBytes;          // kKSlots x kTileBytes
   static constexpr int kV = kK + kKSlots * kTileBytes;    // kVSlots x kTileBytes
   static constexpr int kBar = kV + kVSlots * kTileBytes;
-  static constexpr int kNumBars = 4 + 2 * kKSlots + 2 * kVSlots + 14;
+  static constexpr int kNumBars = 4 + 2 * kKSlots + 2 * kVSlots + 12;
   static constexpr int kSched = kBar + kNumBars * 8;  // int[6]: ring[2], share[2][2]
   static constexpr int kTmemSlot = kSched + 32;
   static constexpr int kBytes = kTmemSlot + 16;
 };
 
 // q_full[2] q_empty[2] k_full[KS] k_empty[KS] v_full[VS] v_empty[VS] s_full[2]
-// s_free[2] p_full[2] pv_done[2] o_free[2] sched_full[2] sched_empty[2]
+// p_full[2] pv_done[2] o_free[2] sched_full[2] sched_empty[2]
 template <int KS, int VS>
 struct FwdBars {
   uint32_t b;
@@ -103,12 +101,11 @@ struct FwdBars {
   __device__ uint32_t v_full(int s) const { return b + 8 * (4 + 2 * KS + s); }
   __device__ uint32_t v_empty(int s) const { return b + 8 * (4 + 2 * KS + VS + s); }
   __device__ uint32_t s_full(int t) const { return b + 8 * (kT + t); }
-  __device__ uint32_t s_free(int t) const { return b + 8 * (kT + 2 + t); }
-  __device__ uint32_t p_full(int t) const { return b + 8 * (kT + 4 + t); }
-  __device__ uint32_t pv_done(int t) const { return b + 8 * (kT + 6 + t); }
-  __device__ uint32_t o_free(int t) const { return b + 8 * (kT + 8 + t); }
-  __device__ uint32_t sched_full(int s) const { return b + 8 * (kT + 10 + s); }
-  __device__ uint32_t sched_empty(int s) const { return b + 8 * (kT + 12 + s); }
+  __device__ uint32_t p_full(int t) const { return b + 8 * (kT + 2 + t); }
+  __device__ uint32_t pv_done(int t) const { return b + 8 * (kT + 4 + t); }
+  __device__ uint32_t o_free(int t) const { return b + 8 * (kT + 6 + t); }
+  __device__ uint32_t sched_full(int s) const { return b + 8 * (kT + 8 + s); }
+  __device__ uint32_t sched_empty(int s) const { return b + 8 * (kT + 10 + s); }
 };
 
 // The 128 threads of softmax warpgroup t.
@@ -159,8 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) record_failure(p.status, kStatusLayout, kSiteFwdSmemAlign);
     return;
   }
-  const uint32_t sQ = smem_u32(smem + L::kQ), sP = smem_u32(smem + L::kP),
-                 sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+  const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK),
+                 sV = smem_u32(smem + L::kV);
   // [0, 2): the item ring; [2 + 2t, 4 + 2t): the item as warpgroup t shares it
   volatile int* sched = reinterpret_cast<volatile int*>(smem + L::kSched);
   const FwdBars<KS, VS> bar{smem_u32(smem + L::kBar)};
@@ -175,7 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar.q_full(t), 1);
       mbar_init(bar.q_empty(t), 1);
       mbar_init(bar.s_full(t), 1);
-      mbar_init(bar.s_free(t), 4);
       mbar_init(bar.p_full(t), 4);
       mbar_init(bar.pv_done(t), 1);
       mbar_init(bar.o_free(t), 4);
@@ -184,11 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < KS; ++s) {
       mbar_init(bar.k_full(s), 1);
-      mbar_init(bar.k_empty(s), 2);
+      mbar_init(bar.k_empty(s), 1);
     }
     for (int s = 0; s < VS; ++s) {
       mbar_init(bar.v_full(s), 1);
-      mbar_init(bar.v_empty(s), 2);
+      mbar_init(bar.v_empty(s), 1);
     }
     fence_barrier_init();
   }
@@ -232,9 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // Registers: the two softmax warpgroups hold a 128-key row of S each; the
-  // producer / MMA warpgroups (warps 8-15) need few. Each warpgroup changes its
+  // producer / MMA warpgroup (warps 8-11) needs few. Each warpgroup changes its
   // own limit at the top of its branch. The split fits the launch's pool of
-  // 512 x 128: 256 x 200 + 256 x 56 = 65536 (the host checks the kernel's
+  // 384 x 168: 256 x 208 + 128 x 88 = 64512 (the host checks the kernel's
   // register count before launching).
   if (warp >= 8) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther) : "memory");
@@ -325,115 +321,136 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 9 || warp == 11) {
-    // ------------------------------------------------------------ S issuer of tile t
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer (both tiles)
+    // One thread issues every product in the order, per step j of the merged
+    // list, S_0(j), O_1 += P_1 V (previous step of tile 1), S_1(j),
+    // O_0 += P_0 V (step j): while one tile's softmax runs, the tensor pipe
+    // holds the other tile's products, so the two softmax warpgroups
+    // alternate. S_t(j) overwrites the TMEM columns the previous P_t V read, so
+    // it waits for that product to complete.
     if (lane == 0) {
-      const int t = warp == 9 ? 0 : 1;
       constexpr uint32_t idesc_s = kFp8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, 0, 1);
       constexpr int kSSteps = kFp8 ? D / 32 : D / 16;  // K steps of S = Q K^T
+      constexpr int kPvSteps = kFp8 ? 4 : 8;           // K steps (keys) of O += P V
       // Shared-memory descriptors are built once: the address field (bits
       // 0-13, in 16-byte units) of every operand stays below 2^14 here, so a
       // descriptor for base + off is the base descriptor plus off / 16.
-      const uint64_t dq = sdesc_sw128(sQ + t * L::kTileBytes, 16, 1024);
+      const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dq1 = sdesc_sw128(sQ + L::kTileBytes, 16, 1024);
       const uint64_t dk_base = sdesc_sw128(sK, 16, 1024);
-      const uint32_t ts = tmem + col_s(t);
-      bool ok = true;
-      int J = 0, ns = 0;  // running step; S products of this tile so far
-      for (int k = 0; ok; ++k) {
-        const int n = read_item(k, ok);
-        if (n < 0) break;
-        const Item it = decode(n);
-        if (!mbar_wait(bar.q_full(t), k & 1, p.status)) {
-          record_failure(p.status, kStatusTimeout, kSiteFwdQ);
-          break;
-        }
-        // the last step of the item this tile visits: Q_t is free for the
-        // next item once that step's S_t has completed (usually found at once:
-        // the list's last entry, or the one before it)
-        int last = it.count - 1;
-        while (last >= 0 && label(it.list[last], t) == FM_TILE_FULL) --last;
-        if (last < 0) mma_commit(bar.q_empty(t));
-        for (int j = 0; ok && j < it.count; ++j, ++J) {
-          const int ks = J % KS;
-          ok = mbar_wait(bar.k_full(ks), (J / KS) & 1, p.status);
-          if (!ok) break;
-          if (label(it.list[j], t) == FM_TILE_FULL) {
-            mbar_arrive(bar.k_empty(ks));  // not visited by this tile
-            continue;
-          }
-          // the softmax has read the previous S_t out of TMEM
-          if (ns > 0 && !(ok = mbar_wait(bar.s_free(t), (ns - 1) & 1, p.status))) break;
-          tc_fence_after();
-          const uint64_t kd = dk_base + static_cast<uint64_t>((ks * L::kTileBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kSSteps; ++kk) {
-            // 32 bytes of each 128-byte row per K step (16 bf16 or 32 e4m3)
-            const uint64_t off16 =
-                static_cast<uint64_t>(((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4);
-            if constexpr (kFp8)
-              mma_ss_f8(ts, dq + off16, kd + off16, idesc_s, kk > 0);
-            else
-              mma_ss(ts, dq + off16, kd + off16, idesc_s, kk > 0);
-          }
-          mma_commit(bar.s_full(t));
-          mma_commit(bar.k_empty(ks));
-          if (j == last) mma_commit(bar.q_empty(t));
-          ++ns;
-        }
-        if (!ok) record_failure(p.status, kStatusTimeout, kSiteFwdK);
-      }
-    }
-  } else if (warp == 12 || warp == 13) {
-    // ------------------------------------------------------------ P V issuer of tile t
-    if (lane == 0) {
-      const int t = warp - 12;
-      constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, 0, 1);
-      constexpr int kPvSteps = kFp8 ? 4 : 8;  // K steps (keys) of O += P V
-      const uint64_t dp = sdesc_sw128(sP + t * L::kPBytes, 16, 1024);  // P, K-major
       // V is MN-major [keys][d] in bf16, K-major [d][keys] as e4m3 V^T
       const uint64_t dv_base = kFp8 ? sdesc_sw128(sV, 16, 1024) : sdesc_sw128(sV, 16384, 1024);
-      const uint32_t to = tmem + col_o(t);
       bool ok = true;
-      int J = 0, nv = 0;  // running step; P V products of this tile so far
+      int J0 = 0;                // running step of the item's first entry
+      int nv[2] = {0, 0};        // P V products per tile so far
+      // S_t of step J into TMEM (K of step J has landed); the previous P_t V
+      // must have completed
+      auto issue_s = [&](int t, int J) -> bool {
+        if (nv[t] > 0 && !mbar_wait(bar.pv_done(t), (nv[t] - 1) & 1, p.status)) return false;
+        tc_fence_after();
+        const uint64_t dq = t == 0 ? dq0 : dq1;
+        const uint64_t kd = dk_base + static_cast<uint64_t>(((J % KS) * L::kTileBytes) >> 4);
+        const uint32_t ts = tmem + col_s(t);
+#pragma unroll
+        for (int kk = 0; kk < kSSteps; ++kk) {
+          // 32 bytes of each 128-byte row per K step (16 bf16 or 32 e4m3)
+          const uint64_t off16 = static_cast<uint64_t>(((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4);
+          if constexpr (kFp8)
+            mma_ss_f8(ts, dq + off16, kd + off16, idesc_s, kk > 0);
+          else
+            mma_ss(ts, dq + off16, kd + off16, idesc_s, kk > 0);
+        }
+        mma_commit(bar.s_full(t));
+        return true;
+      };
+      // O_t += P_t V of step J once P_t is in TMEM and V has landed; the item's
+      // first product overwrites O_t after the previous item's O_t was read out
+      auto issue_pv = [&](int t, int J, bool first, int k) -> bool {
+        const int vs = J % VS;
+        if (!mbar_wait(bar.p_full(t), nv[t] & 1, p.status) ||
+            !mbar_wait(bar.v_full(vs), (J / VS) & 1, p.status) ||
+            (first && k > 0 && !mbar_wait(bar.o_free(t), (k - 1) & 1, p.status)))
+          return false;
+        tc_fence_after();
+        const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
+        const uint32_t ts = tmem + col_s(t), to = tmem + col_o(t);
+#pragma unroll
+        for (int kk = 0; kk < kPvSteps; ++kk) {
+          // A: P, 8 TMEM columns per K step; B: the next 16 key rows of V
+          // (bf16) or the next 32 key bytes of each row of V^T (e4m3)
+          if constexpr (kFp8)
+            mma_ts_f8(to, ts + 8 * kk, vd + static_cast<uint64_t>((kk * 32) >> 4), idesc_pv,
+                      (!first || kk > 0));
+          else
+            mma_ts(to, ts + 8 * kk, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
+                   (!first || kk > 0));
+        }
+        mma_commit(bar.pv_done(t));
+        ++nv[t];
+        return true;
+      };
       for (int k = 0; ok; ++k) {
         const int n = read_item(k, ok);
         if (n < 0) break;
         const Item it = decode(n);
-        bool first = true;  // the item's first product overwrites O_t
-        for (int j = 0; ok && j < it.count; ++j, ++J) {
-          const int vs = J % VS;
-          ok = mbar_wait(bar.v_full(vs), (J / VS) & 1, p.status);
-          if (!ok) break;
-          if (label(it.list[j], t) == FM_TILE_FULL) {
-            mbar_arrive(bar.v_empty(vs));  // not visited by this tile
-            continue;
-          }
-          // P_t is in shared memory; before the item's first product the
-          // previous item's O_t must have been read out
-          ok = mbar_wait(bar.p_full(t), nv & 1, p.status) &&
-               (!first || k == 0 || mbar_wait(bar.o_free(t), (k - 1) & 1, p.status));
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kPvSteps; ++kk) {
-            // A: 32 bytes of each row of P per K step; B: the next 16 key rows
-            // of V (bf16) or the next 32 key bytes of each row of V^T (e4m3)
-            const uint64_t pa =
-                dp + static_cast<uint64_t>(((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4);
-            if constexpr (kFp8)
-              mma_ss_f8(to, pa, vd + static_cast<uint64_t>((kk * 32) >> 4), idesc_pv,
-                        (!first || kk > 0));
-            else
-              mma_ss(to, pa, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
-                     (!first || kk > 0));
-          }
-          mma_commit(bar.pv_done(t));
-          mma_commit(bar.v_empty(vs));
-          first = false;
-          ++nv;
+        if (!mbar_wait(bar.q_full(0), k & 1, p.status) ||
+            !mbar_wait(bar.q_full(1), k & 1, p.status)) {
+          ok = false;
+          break;
         }
-        if (!ok) record_failure(p.status, kStatusTimeout, kSiteFwdP);
+        // the last step each tile visits: Q_t is free for the next item once
+        // that step's S_t has completed (usually found at once: the list's
+        // last entry, or the one before it)
+        int last[2];
+        for (int t = 0; t < 2; ++t) {
+          last[t] = it.count - 1;
+          while (last[t] >= 0 && label(it.list[last[t]], t) == FM_TILE_FULL) --last[t];
+          if (last[t] < 0) mma_commit(bar.q_empty(t));
+        }
+        bool first[2] = {true, true};
+        int pend1 = -1;  // step of tile 1 whose P V is still to be issued
+        for (int j = 0; ok && j < it.count; ++j) {
+          const int J = J0 + j, entry = it.list[j];
+          const bool a0 = label(entry, 0) != FM_TILE_FULL, a1 = label(entry, 1) != FM_TILE_FULL;
+          ok = mbar_wait(bar.k_full(J % KS), (J / KS) & 1, p.status);
+          if (ok && a0) {
+            ok = issue_s(0, J);
+            if (ok && j == last[0]) mma_commit(bar.q_empty(0));
+          }
+          if (ok && pend1 >= 0) {
+            // tile 1's previous step: its V slot is released after this product
+            ok = issue_pv(1, pend1, first[1], k);
+            if (ok) mma_commit(bar.v_empty(pend1 % VS));
+            first[1] = false;
+            pend1 = -1;
+          }
+          if (ok && a1) {
+            ok = issue_s(1, J);
+            if (ok && j == last[1]) mma_commit(bar.q_empty(1));
+            pend1 = J;
+          }
+          if (ok) mma_commit(bar.k_empty(J % KS));  // both tiles' S of this step issued
+          if (ok && a0) {
+            ok = issue_pv(0, J, first[0], k);
+            first[0] = false;
+          }
+          // V of this step is released now unless tile 1 still needs it
+          if (ok && !a1) {
+            ok = mbar_wait(bar.v_full(J % VS), (J / VS) & 1, p.status);
+            if (ok) mma_commit(bar.v_empty(J % VS));
+          }
+        }
+        if (ok && pend1 >= 0) {
+          ok = issue_pv(1, pend1, first[1], k);
+          if (ok) mma_commit(bar.v_empty(pend1 % VS));
+        }
+        if (!ok) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdP);
+          break;
+        }
+        J0 += it.count;
       }
     }
   }
@@ -510,10 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t sv[128];
           tmem_ld64(ts, ts + 32, *reinterpret_cast<uint32_t(*)[64]>(sv));
           tmem_ld64(ts + 64, ts + 96, *reinterpret_cast<uint32_t(*)[64]>(sv + 64));
-          // S_t is in registers: its TMEM columns may take the next S_t
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar.s_free(t));
           if (partial) {
 #pragma unroll
             for (int jj = 0; jj < 128; ++jj)
@@ -570,33 +583,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_split(la, l0, l1);
           f2_split(lb, l2, l3);
           l = l * alpha + ((l0 + l1) + (l2 + l3));
-          // the previous O_t += P_t V has completed: the P buffer may be
-          // overwritten and O_t is quiescent (the next product waits for this
-          // step's P)
-          if (ns > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(t), (ns - 1) & 1, p.status));
-            if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdO);
-            tc_fence_after();
-          }
-          if (ok) {
-            // the item's first product overwrites O_t, so no rescale then
-            if (!first && __any_sync(0xffffffffu, rescale)) {
+          // P over S_t's own columns: keys [0, 128) as bf16 pairs in columns
+          // [0, 64) (the A operand of P V), or as e4m3 quads in columns [0, 32)
+          tmem_st32p(ts, sv);
+          if constexpr (!kFp8) tmem_st32p(ts + 32, sv + 32);
+          // O_t is quiescent here (its last product completed before S_t was
+          // issued); the item's first product overwrites it, so no rescale then
+          if (!first && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-              for (int ch = 0; ch < D / 32; ++ch) tmem_scale32(to + 32 * ch, alpha);
-              tmem_st_wait();
-            }
-            // P_t row `row` in the 128-byte-swizzled K-major layout of the A
-            // operand: 128 keys as bf16 pairs (two 128-byte chunks) or as
-            // e4m3 quads (one chunk), 16 bytes per store
-            const uint32_t prow = sP + t * L::kPBytes;
-#pragma unroll
-            for (int c16 = 0; c16 < (kFp8 ? 8 : 16); ++c16)
-              st_shared_v4(prow + (c16 >> 3) * L::kChunk + sw128_offset(row, c16 & 7),
-                           sv[4 * c16], sv[4 * c16 + 1], sv[4 * c16 + 2], sv[4 * c16 + 3]);
-            fence_proxy_async_smem();  // visible to the tensor cores' reads
+            for (int ch = 0; ch < D / 32; ++ch) tmem_scale32(to + 32 * ch, alpha);
           }
-        } else if (lane == 0) {
-          mbar_arrive(bar.s_free(t));  // keep the handshake after a failure
+          tmem_st_wait();
         }
         tc_fence_before();
         __syncwarp();
