@@ -110,21 +110,14 @@ typedef struct {
  *   col_count int32  [B,Hm,Tc]           non-FULL tiles per key block
  *   col_list  int32  [B,Hm,Tc,Tr]        (query block << 2) | label, ascending
  *   col_order int32  [B,Hm,Tc]           key blocks by descending col_count
- *   pair_count int32 [B,Hm,Tp]           key blocks visited by the pair of query
- *                                       blocks (2p, 2p+1): non-FULL for either
- *   pair_list int32  [B,Hm,Tp,Tc]        (key block << 4) | (label of 2p << 2) |
- *                                       label of 2p+1, ascending; FM_TILE_FULL marks
- *                                       the block not visited (and every entry of a
- *                                       block 2p+1 >= Tr)
- *   pair_order int32 [B,Hm,Tp]           pairs by descending pair_count
  *   lse2      fp32   [B,H,Npad]   [bwd]  LSE * log2(e) (+inf for a fully masked
  *                                       row and for the padding rows n >= N)
  *   delta     fp32   [B,H,Npad]   [bwd]  rowsum(dO * O) (0 on padding rows)
  *   dq_accum  fp32   [B,H,Npad,d] [bwd]  dQ accumulator
- * with Tr = Tc = ceil(N / 128), Tp = ceil(Tr / 2) and Npad = 128 * Tr. */
+ * with Tr = Tc = ceil(N / 128) and Npad = 128 * Tr. */
 typedef struct {
   size_t status, minmax, labels, labels_t, row_count, row_list, row_order, col_count, col_list,
-      col_order, pair_count, pair_list, pair_order, lse2, delta, dq_accum, total;
+      col_order, lse2, delta, dq_accum, total;
 } fm_ws_layout;
 
 /* Workspace size in bytes for the given problem; 0 for an unsupported shape. */
@@ -182,7 +175,7 @@ fm_status flashmask_bwd_finalize(int B, int H, int Hm, int N, int d, float scale
  * 0), but the classification tables live in a fixed scratch array of
  * FM_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
  * library holds until the process exits. Shapes whose tables would not fit
- * (about B*Hm*(N/128)^2*12 bytes; N = 131072 with B*Hm = 1 fits) return
+ * (about B*Hm*(N/128)^2*10 bytes; N = 131072 with B*Hm = 1 fits) return
  * FM_ERR_WORKSPACE before anything is launched. The call allocates nothing:
  * no cudaMalloc, no cudaFree, no allocating library routine.
  *   - The first call on each device looks up the scratch array's device

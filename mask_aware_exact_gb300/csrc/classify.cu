@@ -23,10 +23,9 @@
 //
 // The same pass writes the per-key-block min/max of each vector, the labels in
 // both tile orders, the ascending lists of non-FULL tiles per key block and
-// (second kernel) per query block, (third kernel) the merged lists of each
-// pair of adjacent query blocks, which the forward processes together, and
-// (fourth kernel) each block and pair index ranked by descending amount of
-// work, which the attention kernels use as their launch order (longest first).
+// (second kernel) per query block, and (third kernel) each block index ranked
+// by descending amount of work, which the attention kernels use as their
+// launch order (longest first).
 #include <climits>
 
 #include "internal.h"
@@ -200,47 +199,19 @@ __global__ void __launch_bounds__(128) classify_rows_kernel(int Tr, int Tc, Clas
   if (tid == 0) t.row_count[static_cast<size_t>(bm) * Tr + r] = carry;
 }
 
-// One block per pair of query blocks (2p, 2p + 1): the ascending list of key
-// blocks that are non-FULL for either of the two, each entry carrying both
-// labels (a block 2p + 1 >= Tr counts as FULL everywhere).
-__global__ void __launch_bounds__(128) classify_pairs_kernel(int Tr, int Tc, int Tp,
-                                                             ClassifyTables t) {
-  __shared__ int warp_tot[4];
-  const int p = blockIdx.x, bm = blockIdx.y, tid = threadIdx.x;
-  const int r0 = 2 * p, r1 = 2 * p + 1;
-  const uint8_t* lab0 = t.labels + (static_cast<size_t>(bm) * Tr + r0) * Tc;
-  const uint8_t* lab1 = t.labels + (static_cast<size_t>(bm) * Tr + r1) * Tc;
-  int32_t* list = t.pair_list + (static_cast<size_t>(bm) * Tp + p) * Tc;
-  int carry = 0;
-  for (int c0 = 0; c0 < Tc; c0 += kTile) {
-    const int c = c0 + tid;
-    const int a = c < Tc ? lab0[c] : FM_TILE_FULL;
-    const int b = (c < Tc && r1 < Tr) ? lab1[c] : FM_TILE_FULL;
-    const int keep = (a != FM_TILE_FULL || b != FM_TILE_FULL) ? 1 : 0;
-    int tot;
-    const int pos = block_scan128(keep, warp_tot, tot) - keep + carry;
-    carry += tot;
-    if (keep) list[pos] = (c << 4) | (a << 2) | b;
-  }
-  if (tid == 0) t.pair_count[static_cast<size_t>(bm) * Tp + p] = carry;
-}
-
 // Ranks block indices by descending count (ties: ascending index) and writes
-// order[rank] = index. blockIdx.y = 0 ranks query blocks, 1 key blocks, 2
-// pairs of query blocks; blockIdx.z takes indices [256 z, 256 z + 256).
-__global__ void __launch_bounds__(256) classify_order_kernel(int Tr, int Tc, int Tp,
-                                                             ClassifyTables t) {
+// order[rank] = index. blockIdx.y = 0 ranks query blocks, 1 key blocks;
+// blockIdx.z takes indices [256 z, 256 z + 256).
+__global__ void __launch_bounds__(256) classify_order_kernel(int Tr, int Tc, ClassifyTables t) {
   extern __shared__ int cnt[];
   const int bm = blockIdx.x;
   const int which = blockIdx.y;
   const int i0 = blockIdx.z * blockDim.x;
-  const int n = which == 0 ? Tr : (which == 1 ? Tc : Tp);
-  const int32_t* src = which == 0   ? t.row_count + static_cast<size_t>(bm) * Tr
-                       : which == 1 ? t.col_count + static_cast<size_t>(bm) * Tc
-                                    : t.pair_count + static_cast<size_t>(bm) * Tp;
-  int32_t* order = which == 0   ? t.row_order + static_cast<size_t>(bm) * Tr
-                   : which == 1 ? t.col_order + static_cast<size_t>(bm) * Tc
-                                : t.pair_order + static_cast<size_t>(bm) * Tp;
+  const int n = which == 0 ? Tr : Tc;
+  const int32_t* src = which == 0 ? t.row_count + static_cast<size_t>(bm) * Tr
+                                  : t.col_count + static_cast<size_t>(bm) * Tc;
+  int32_t* order = which == 0 ? t.row_order + static_cast<size_t>(bm) * Tr
+                              : t.col_order + static_cast<size_t>(bm) * Tc;
   for (int i = threadIdx.x; i < n; i += blockDim.x) cnt[i] = src[i];
   __syncthreads();
   {
@@ -260,7 +231,7 @@ __global__ void __launch_bounds__(256) classify_order_kernel(int Tr, int Tc, int
 
 cudaError_t launch_classify(const MaskDev& m, int B, int N, const ClassifyTables& t,
                             cudaStream_t s) {
-  const int Tr = (N + kTile - 1) / kTile, Tc = Tr, Tp = (Tr + 1) / 2;
+  const int Tr = (N + kTile - 1) / kTile, Tc = Tr;
   const int BHm = B * m.Hm;
   const size_t sh_cols = static_cast<size_t>(2) * (Tr + 1) * sizeof(int);
   const size_t sh_order = static_cast<size_t>(Tr) * sizeof(int);
@@ -277,8 +248,7 @@ cudaError_t launch_classify(const MaskDev& m, int B, int N, const ClassifyTables
   }
   classify_cols_kernel<<<dim3(Tc, BHm), 128, sh_cols, s>>>(m, N, Tr, Tc, t);
   classify_rows_kernel<<<dim3(Tr, BHm), 128, 0, s>>>(Tr, Tc, t);
-  classify_pairs_kernel<<<dim3(Tp, BHm), 128, 0, s>>>(Tr, Tc, Tp, t);
-  classify_order_kernel<<<dim3(BHm, 3, (Tr + 255) / 256), 256, sh_order, s>>>(Tr, Tc, Tp, t);
+  classify_order_kernel<<<dim3(BHm, 2, (Tr + 255) / 256), 256, sh_order, s>>>(Tr, Tc, t);
   return cudaGetLastError();
 }
 

@@ -58,13 +58,6 @@ fm_ws_layout make_layout(int B, int H, int Hm, int N, int d, int for_bwd) {
   off = align_up(off + BHm * Tc * Tr * 4, 256);
   L.col_order = off;
   off = align_up(off + BHm * Tc * 4, 256);
-  const size_t Tp = (Tr + 1) / 2;
-  L.pair_count = off;
-  off = align_up(off + BHm * Tp * 4, 256);
-  L.pair_list = off;
-  off = align_up(off + BHm * Tp * Tc * 4, 256);
-  L.pair_order = off;
-  off = align_up(off + BHm * Tp * 4, 256);
   if (for_bwd) {
     L.lse2 = off;
     off = align_up(off + BHN * 4, 256);
@@ -89,9 +82,6 @@ fm::ClassifyTables tables(const fm_ws_layout& L, void* ws) {
   t.col_count = reinterpret_cast<int32_t*>(w + L.col_count);
   t.col_list = reinterpret_cast<int32_t*>(w + L.col_list);
   t.col_order = reinterpret_cast<int32_t*>(w + L.col_order);
-  t.pair_count = reinterpret_cast<int32_t*>(w + L.pair_count);
-  t.pair_list = reinterpret_cast<int32_t*>(w + L.pair_list);
-  t.pair_order = reinterpret_cast<int32_t*>(w + L.pair_order);
   return t;
 }
 
@@ -294,10 +284,9 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
   p.Tc = blocks_of(N);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.qscale = p.kscale = p.vscale = nullptr;
-  p.Tp = (p.Tr + 1) / 2;
-  p.pair_count = t.pair_count;
-  p.pair_list = t.pair_list;
-  p.pair_order = t.pair_order;
+  p.row_count = t.row_count;
+  p.row_list = t.row_list;
+  p.row_order = t.row_order;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.status = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.status);
@@ -372,10 +361,9 @@ fm_status flashmask_fwd_fp8(const void* q, const void* k, const void* v, const f
   p.qscale = f.qscale;
   p.kscale = f.kscale;
   p.vscale = f.vscale;
-  p.Tp = (p.Tr + 1) / 2;
-  p.pair_count = t.pair_count;
-  p.pair_list = t.pair_list;
-  p.pair_order = t.pair_order;
+  p.row_count = t.row_count;
+  p.row_list = t.row_list;
+  p.row_order = t.row_order;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
   p.status = reinterpret_cast<int32_t*>(w + F.base.status);

@@ -1,47 +1,41 @@
-// Forward kernel: exact attention over the non-FULL tiles of a pair of 128-row
-// query blocks ("FlashMask: Efficient and Rich Mask Extension of
-// FlashAttention", abstract: skip masked computation, exact result;
-// "FlashAttention-3", abstract: warp specialisation overlapping TMA data
-// movement with tensor-core work, and block-wise matmul interleaved with
-// softmax).
+// Forward kernel: exact attention over the non-FULL tiles of one 128-row query
+// block ("FlashMask: Efficient and Rich Mask Extension of FlashAttention",
+// abstract: skip masked computation, exact result; "FlashAttention-3",
+// abstract: warp specialisation overlapping TMA data movement with tensor-core
+// work, and block-wise matmul interleaved with softmax).
 //
-// A work item is one head's pair of adjacent query blocks (r0, r1) = (2p,
-// 2p + 1). Both tiles walk the merged list of key blocks that are non-FULL for
-// either of them; each K and V block is loaded once and serves both. Each tile
-// t has one chain through the tensor cores and TMEM,
+// The non-FULL key blocks of the query block are visited one per step. The
+// tensor cores run ahead of the softmax: S_{j+3} = Q K_{j+3}^T is issued as
+// soon as O += P_j V_j (the last reader of its TMEM region) has completed, so
+// the S products stay off the chain softmax_j -> O += P_j V_j, and the
+// softmax warps find S_{j+1} ready when they finish step j. P_j is written
+// over S_j's own region.
 //
-//     S_t = Q_t K_j^T -> softmax_t (P_t over S_t) -> O_t += P_t V_j -> S_t of the next block,
+// Persistent CTAs (one per SM) take query blocks from a work counter; see the
+// kernel's comment. Warp roles (384 threads):
+//   warps 0-7  softmax, two warpgroups. Thread (w, r) owns query row r (= TMEM
+//              lane r) and key columns [64w, 64w+64) of every block: it loads
+//              its 64 S values into registers, applies the element mask on
+//              PARTIAL tiles, exchanges its partial row maximum with the other
+//              warpgroup through shared memory, keeps the running max and
+//              partial sum in fp32 (log2 domain), and writes its P slice into
+//              TMEM. O is rescaled only when the max grows by more than 2^8
+//              (lazy rescaling: exact after the final division); warpgroup w
+//              rescales O columns [w d/2, (w+1) d/2). Finally O = acc / l and LSE.
+//   warp 8     work scheduler and TMA producer of Q (once per item) and K
+//              blocks (three-slot ring).
+//   warp 9     MMA issuer (one thread): per step O += P_j V_j after go(j), then
+//              S_{j+3} once that product has completed and K_{j+3} has landed.
+//   warp 10    TMA producer of V blocks (three-slot ring).
+//   warp 11    gatekeeper (one thread): for step j waits until V_j has landed,
+//              P_j is written (and, at an item's first step, the previous O
+//              has been read out), then signals go(j), so that the MMA thread
+//              waits once per product.
 //
-// and one softmax warpgroup. A single thread issues both tiles' products in the
-// order S_0(j), O_1 += P_1 V (tile 1's previous step), S_1(j), O_0 += P_0 V
-// (step j), so that while one tile's softmax works the tensor pipe holds the
-// other tile's products and the two softmax warpgroups take turns. P stays in
-// TMEM (the A operand of P V), which keeps the shared-memory traffic of a step
-// to the Q K^T operands and V: with both operands of an M = N = 128 product in
-// shared memory the tensor cores' shared-memory reads (about 128 bytes per
-// clock) are already the limit. A tile skips the key blocks that are FULL for
-// it.
-//
-// Persistent CTAs (one per SM) take items from a work counter in the
-// workspace, head-major (a head's K and V stay in L2 while its pairs run) and
-// longest pair first within a head. Warp roles (384 threads):
-//   warps 0-3   softmax of tile 0: thread = query row = TMEM lane, the whole
-//               128-key row of S in registers: element mask on PARTIAL tiles,
-//               row maximum, exponentials (log2 domain), row sum, P as bf16 (or
-//               e4m3) over S_t. O_t is rescaled only when the maximum grows by
-//               more than 2^8 (lazy rescaling, exact after the final division).
-//               Epilogue: O_t / l, LSE.
-//   warps 4-7   softmax of tile 1.
-//   warp 8      work scheduler; TMA producer of Q_0, Q_1 (once per item) and
-//               of the K ring.
-//   warp 9      MMA issuer of both tiles (one thread).
-//   warp 10     TMA producer of the V ring.
-//   warp 11     idle (completes the register-split warpgroup).
-//
-// TMEM columns (512): S_0/P_0 [0,128), S_1/P_1 [128,256), O_0 [256,256+d),
-// O_1 [384,384+d). S_t of the next block is issued only after O_t += P_t V
-// has completed (the product reads P_t from S_t's columns), so by the time the
-// softmax sees S_t complete, O_t is quiescent and may be rescaled in place.
+// TMEM columns (512 allocated): S regions [0,128) [128,256) [256,384), O [384, 384+d).
+// Ordering: S_{j+3} reuses the region of S_j / P_j once O += P_j V_j has
+// completed; the softmax of step j rescales O only after O += P_{j-1} V_{j-1}
+// has completed.
 #include "internal.h"
 #include "ptx.cuh"
 #include "ptx_fp8.cuh"
@@ -52,105 +46,141 @@ namespace fm {
 namespace {
 
 constexpr int kThreads = 384;
+constexpr int kSRegions = 3;  // TMEM S/P regions of 128 columns
+constexpr int kKSlots = 3, kVSlots = 3;
+constexpr uint32_t kColO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // FP8: P is stored as e4m3(p * kFp8PScale). With the running maximum lagging
 // by at most kRescaleThresholdFp8 (log2 units), p < 2^threshold and
 // p * kFp8PScale stays below 448, the largest finite e4m3 value.
 constexpr float kRescaleThresholdFp8 = 4.0f;
 constexpr float kFp8PScale = 28.0f;
-// Roles that read each published work item: the MMA warp, the V producer and
-// the first warp of each softmax warpgroup (which shares it with the other
-// three through shared memory).
-constexpr int kSchedReaders = 4;
-// Per-thread register limits after the split (setmaxnreg): softmax warpgroups,
-// producer / MMA warpgroup. Their sum over the 384 threads must not exceed the
-// pool the CTA is launched with (threads x registers of the compiled kernel).
-constexpr int kRegsSoftmax = 208, kRegsOther = 88;
-constexpr int kRegPool = 256 * kRegsSoftmax + 128 * kRegsOther;
-
-__device__ __forceinline__ uint32_t col_s(int t) { return 128u * static_cast<uint32_t>(t); }
-__device__ __forceinline__ uint32_t col_o(int t) { return 256u + 128u * static_cast<uint32_t>(t); }
 
 template <int D, bool kFp8>
 struct FwdLayout {
   static constexpr int kTileBytes = kTile * D * (kFp8 ? 1 : 2);  // one 128 x d tile
   static constexpr int kChunks = kFp8 ? 1 : D / 64;  // 128-byte-wide TMA boxes per tile
   static constexpr int kChunk = 16384;              // 128 rows x 128 bytes
-  static constexpr int kKSlots = kTileBytes >= 32768 ? 3 : 4;
-  static constexpr int kVSlots = kTileBytes >= 32768 ? 2 : 4;
-  static constexpr int kQ = 0;                            // Q_0, Q_1
-  static constexpr int kK = kQ + 2 * kTileBytes;          // kKSlots x kTileBytes
-  static constexpr int kV = kK + kKSlots * kTileBytes;    // kVSlots x kTileBytes
-  static constexpr int kBar = kV + kVSlots * kTileBytes;
-  static constexpr int kNumBars = 4 + 2 * kKSlots + 2 * kVSlots + 12;
-  static constexpr int kSched = kBar + kNumBars * 8;  // int[6]: ring[2], share[2][2]
-  static constexpr int kTmemSlot = kSched + 32;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;             // kKSlots x kTileBytes
+  static constexpr int kV = kK + kKSlots * kTileBytes;   // kVSlots x kTileBytes
+  static constexpr int kRed = kV + kVSlots * kTileBytes;  // fp32 [2 parity][2 groups][128]
+  static constexpr int kBar = kRed + 2 * 2 * kTile * 4;
+  // q_full, k_full[3], v_full[3], s_full[3], p_full[3], pv_done[3], go[3],
+  // sched_full[2], sched_empty[2], o_free. K slot, V slot and S region of step
+  // J are all J % 3, so "S_J done" also frees K slot J % 3 and "P_J V_J done"
+  // also frees V slot J % 3.
+  static_assert(kKSlots == kSRegions && kVSlots == kSRegions, "slots follow the S regions");
+  static constexpr int kNumBars = 1 + kKSlots + kVSlots + 4 * kSRegions + 5;
+  static constexpr int kSched = kBar + kNumBars * 8;  // int[4]
+  static constexpr int kTmemSlot = kSched + 16;
   static constexpr int kBytes = kTmemSlot + 16;
 };
 
-// q_full[2] q_empty[2] k_full[KS] k_empty[KS] v_full[VS] v_empty[VS] s_full[2]
-// p_full[2] pv_done[2] o_free[2] sched_full[2] sched_empty[2]
-template <int KS, int VS>
 struct FwdBars {
-  uint32_t b;
-  static constexpr int kT = 4 + 2 * KS + 2 * VS;
-  __device__ uint32_t q_full(int t) const { return b + 8 * t; }
-  __device__ uint32_t q_empty(int t) const { return b + 8 * (2 + t); }
-  __device__ uint32_t k_full(int s) const { return b + 8 * (4 + s); }
-  __device__ uint32_t k_empty(int s) const { return b + 8 * (4 + KS + s); }
-  __device__ uint32_t v_full(int s) const { return b + 8 * (4 + 2 * KS + s); }
-  __device__ uint32_t v_empty(int s) const { return b + 8 * (4 + 2 * KS + VS + s); }
-  __device__ uint32_t s_full(int t) const { return b + 8 * (kT + t); }
-  __device__ uint32_t p_full(int t) const { return b + 8 * (kT + 2 + t); }
-  __device__ uint32_t pv_done(int t) const { return b + 8 * (kT + 4 + t); }
-  __device__ uint32_t o_free(int t) const { return b + 8 * (kT + 6 + t); }
-  __device__ uint32_t sched_full(int s) const { return b + 8 * (kT + 8 + s); }
-  __device__ uint32_t sched_empty(int s) const { return b + 8 * (kT + 10 + s); }
+  uint32_t base;
+  __device__ uint32_t q_full() const { return base; }
+  __device__ uint32_t k_full(int s) const { return base + 8 * (1 + s); }
+  __device__ uint32_t v_full(int s) const { return base + 8 * (1 + kKSlots + s); }
+  __device__ uint32_t s_full(int r) const { return base + 8 * (1 + kKSlots + kVSlots + r); }
+  __device__ uint32_t p_full(int r) const {
+    return base + 8 * (1 + kKSlots + kVSlots + kSRegions + r);
+  }
+  __device__ uint32_t pv_done(int r) const {
+    return base + 8 * (1 + kKSlots + kVSlots + 2 * kSRegions + r);
+  }
+  __device__ uint32_t go(int r) const {
+    return base + 8 * (1 + kKSlots + kVSlots + 3 * kSRegions + r);
+  }
+  __device__ uint32_t sched_full(int s) const {
+    return base + 8 * (1 + kKSlots + kVSlots + 4 * kSRegions + s);
+  }
+  __device__ uint32_t sched_empty(int s) const {
+    return base + 8 * (3 + kKSlots + kVSlots + 4 * kSRegions + s);
+  }
+  __device__ uint32_t o_free() const { return base + 8 * (5 + kKSlots + kVSlots + 4 * kSRegions); }
 };
 
-// The 128 threads of softmax warpgroup t.
-__device__ __forceinline__ void group_bar(int t) {
-  asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
-}
+// Roles that read each published work item: the MMA issuer, the V producer,
+// the gatekeeper and softmax warp 0 (which shares it with the other seven).
+constexpr int kSchedReaders = 4;
 
-// Multiplies 32 consecutive TMEM columns of this warp's lanes by f.
-__device__ __forceinline__ void tmem_scale32(uint32_t taddr, float f) {
-  uint32_t v[32];
-  tmem_ld32(taddr, v);
+
+// The 256 softmax threads (both warpgroups).
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Multiplies kOCols (16 or 32) consecutive TMEM columns of this warp's lanes by f.
+template <int n>
+__device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, float f) {
+  if constexpr (n == 32) {
+    uint32_t v[32];
+    tmem_ld32(taddr, v);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-  tmem_st32(taddr, v);
+    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+    tmem_st32(taddr, v);
+  } else {
+    uint32_t v[16];
+    tmem_ld16(taddr, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+    tmem_st16(taddr, v);
+  }
 }
 
-// Writes 32 TMEM columns of this lane's row, times f, as bf16 (the TMEM load
-// runs on every lane of the warp; only lanes with `store` write).
+// Writes n (16 or 32) TMEM columns of this lane's row, times f, as bf16 (the TMEM
+// load runs on every lane of the warp; only lanes with `store` write).
+template <int n>
 __device__ __forceinline__ void tmem_cols_to_bf16(uint32_t taddr, bool live, float f,
                                                   uint16_t* dst, bool store) {
-  uint32_t v[32];
+  uint32_t v[n];
   if (live) {
-    tmem_ld32(taddr, v);
+    if constexpr (n == 32) {
+      tmem_ld32(taddr, v);
+    } else {
+      tmem_ld16(taddr, v);
+    }
   } else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0u;
+    for (int i = 0; i < n; ++i) v[i] = 0u;
   }
   if (!store) return;  // after the (warp-collective) TMEM load
-  store_row32_bf16(dst, v, f);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < n / 8; ++i) {
+    uint4 q4;
+    q4.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]) * f, __uint_as_float(v[8 * i + 1]) * f);
+    q4.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * f, __uint_as_float(v[8 * i + 3]) * f);
+    q4.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * f, __uint_as_float(v[8 * i + 5]) * f);
+    q4.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * f, __uint_as_float(v[8 * i + 7]) * f);
+    d4[i] = q4;
+  }
 }
 
 // kShortLast: N is not a multiple of 128. kFp8 (d = 128 only): e4m3 Q, K and
 // transposed V with block scales, kind::f8f6f4 MMAs (K = 32 per instruction),
 // P stored as e4m3(p * kFp8PScale).
+//
+// Persistent: one CTA per SM takes work items (one query block of one head)
+// from a global counter until none is left. The Q/K producer claims the items
+// and publishes them to the other roles through a two-entry ring in shared
+// memory. Every role numbers the key blocks it handles with one running step
+// index J across items, so the K, V and S rings, their barriers and the
+// tensor pipe run on from one item into the next: the next item's Q, first K
+// blocks and first S products are loaded and computed while the softmax warps
+// finish the current item. Two hand-offs cross an item boundary: Q is
+// reloaded once the last S of the previous item has completed, and the first
+// O += P V of an item (which overwrites O) waits until the softmax warps have
+// read the previous item's O out of TMEM (o_free).
 template <int D, bool kShortLast, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const FwdParams p) {
   using L = FwdLayout<D, kFp8>;
-  constexpr int KS = L::kKSlots, VS = L::kVSlots;
   static_assert(!kFp8 || D == 128, "the FP8 forward is for d = 128");
-  static_assert(L::kBytes <= 232448, "shared memory");
+  constexpr int kOCols = D / 2;  // O columns per softmax warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_items = p.B * p.H * p.Tp;
+  const int n_items = p.B * p.H * p.Tr;
 
   if ((smem_u32(smem) & 1023u) != 0) {  // 128-byte swizzle atoms need 1024-byte alignment
     if (tid == 0) record_failure(p.status, kStatusLayout, kSiteFwdSmemAlign);
@@ -158,9 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK),
                  sV = smem_u32(smem + L::kV);
-  // [0, 2): the item ring; [2 + 2t, 4 + 2t): the item as warpgroup t shares it
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
+  // [0, 2): the item ring; [2, 4): the item as the softmax warps share it
   volatile int* sched = reinterpret_cast<volatile int*>(smem + L::kSched);
-  const FwdBars<KS, VS> bar{smem_u32(smem + L::kBar)};
+  const FwdBars bar{smem_u32(smem + L::kBar)};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   if (warp == 9) {
@@ -168,51 +199,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar.q_full(t), 1);
-      mbar_init(bar.q_empty(t), 1);
-      mbar_init(bar.s_full(t), 1);
-      mbar_init(bar.p_full(t), 4);
-      mbar_init(bar.pv_done(t), 1);
-      mbar_init(bar.o_free(t), 4);
-      mbar_init(bar.sched_full(t), 1);
-      mbar_init(bar.sched_empty(t), kSchedReaders);
+    mbar_init(bar.q_full(), 1);
+    for (int s = 0; s < kKSlots; ++s) mbar_init(bar.k_full(s), 1);
+    for (int s = 0; s < kVSlots; ++s) mbar_init(bar.v_full(s), 1);
+    for (int g = 0; g < kSRegions; ++g) {
+      mbar_init(bar.s_full(g), 1);
+      mbar_init(bar.p_full(g), 8);
+      mbar_init(bar.pv_done(g), 1);
+      mbar_init(bar.go(g), 1);
     }
-    for (int s = 0; s < KS; ++s) {
-      mbar_init(bar.k_full(s), 1);
-      mbar_init(bar.k_empty(s), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar.sched_full(s), 1);
+      mbar_init(bar.sched_empty(s), kSchedReaders);
     }
-    for (int s = 0; s < VS; ++s) {
-      mbar_init(bar.v_full(s), 1);
-      mbar_init(bar.v_empty(s), 1);
-    }
+    mbar_init(bar.o_free(), 8);
     fence_barrier_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Work item n: head-major, longest pairs of each head first.
+
+  // Work item n: head-major, longest query blocks of each head first, so the
+  // CTAs working at the same time share one head's K and V in L2.
   struct Item {
-    int bh, bm, r0, r1, count;
+    int bh, bm, r, ntiles, head_row0, q_row0;
     const int32_t* list;
   };
   auto decode = [&](int n) -> Item {
     Item it;
-    it.bh = n / p.Tp;
-    const int rank = n % p.Tp;
+    it.bh = n / p.Tr;
+    const int rank = n % p.Tr;
     const int b = it.bh / p.H, h = it.bh % p.H;
     it.bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
-    const size_t base = static_cast<size_t>(it.bm) * p.Tp;
-    const int pair = p.pair_order[base + rank];
-    it.count = p.pair_count[base + pair];
-    it.list = p.pair_list + (base + pair) * p.Tc;
-    it.r0 = 2 * pair;
-    it.r1 = 2 * pair + 1;  // may be Tr: a missing block whose entries are all FULL
+    it.r = p.row_order[static_cast<size_t>(it.bm) * p.Tr + rank];
+    it.ntiles = p.row_count[static_cast<size_t>(it.bm) * p.Tr + it.r];
+    it.list = p.row_list + (static_cast<size_t>(it.bm) * p.Tr + it.r) * p.Tc;
+    it.head_row0 = it.bh * p.N;               // first row of this head in [B*H*N, d]
+    it.q_row0 = it.head_row0 + it.r * kTile;  // first query row of the block
     return it;
   };
-  // Label of tile t in a merged-list entry (FM_TILE_FULL: not visited).
-  auto label = [](int entry, int t) -> int { return t == 0 ? (entry >> 2) & 3 : entry & 3; };
   // The k-th item of this CTA (k = 0, 1, ...) from the ring, or -1 when no
   // item is left or the wait gave up (then `ok` is false).
   auto read_item = [&](int k, bool& ok) -> int {
@@ -227,13 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     return n;
   };
 
-  // Registers: the two softmax warpgroups hold a 128-key row of S each; the
-  // producer / MMA warpgroup (warps 8-11) needs few. Each warpgroup changes its
-  // own limit at the top of its branch. The split fits the launch's pool of
-  // 384 x 168: 256 x 208 + 128 x 88 = 64512 (the host checks the kernel's
-  // register count before launching).
-  if (warp >= 8) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther) : "memory");
   if (warp == 8) {
     // ------------------------------------------------------------ scheduler, TMA producer of Q, K
     if (lane == 0) {
@@ -243,47 +262,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = atomicAdd(p.sched, 1);
         return n < n_items ? n : -1;
       };
+      // K of step J into slot J % 3 once S_{J-3} has completed; kb is the
+      // key block, bh the head (3-D map: rows past the head's end read zeros)
+      auto load_k = [&](int J, int kb, int bh) -> bool {
+        const int slot = J % kKSlots;
+        if (J >= kKSlots &&
+            !mbar_wait(bar.s_full(slot), ((J / kKSlots) - 1) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdKEmpty);
+          return false;
+        }
+        mbar_arrive_expect_tx(bar.k_full(slot), L::kTileBytes);
+        for (int ch = 0; ch < L::kChunks; ++ch)
+          tma_load_3d(sK + slot * L::kTileBytes + ch * L::kChunk, &mk, ch * 64, kb * kTile, bh,
+                      bar.k_full(slot));
+        return true;
+      };
       int cur = claim();
       sched[0] = cur;
       mbar_arrive(bar.sched_full(0));
       bool ok = true;
-      int J = 0;  // running step over the merged lists of this CTA's items
+      int J = 0, J_last = -1;  // running step; last step of the previous item with tiles
       for (int k = 0; ok && cur >= 0; ++k) {
         const Item it = decode(cur);
-        // Q_t of the item once the previous item's S_t products have completed;
-        // a missing second block reloads the first (its products are never issued)
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (k >= 1 && !mbar_wait(bar.q_empty(t), (k - 1) & 1, p.status)) {
+        if (it.ntiles > 0) {
+          // the Q buffer is free once the last S of the previous item is done
+          if (J_last >= 0 && !mbar_wait(bar.s_full(J_last % kSRegions),
+                                        (J_last / kSRegions) & 1, p.status)) {
             record_failure(p.status, kStatusTimeout, kSiteFwdKEmpty);
             ok = false;
             break;
           }
-          const int qb = (t == 1 && it.r1 < p.Tr) ? it.r1 : it.r0;
-          mbar_arrive_expect_tx(bar.q_full(t), L::kTileBytes);
+          mbar_arrive_expect_tx(bar.q_full(), L::kTileBytes);
           for (int ch = 0; ch < L::kChunks; ++ch)
-            tma_load_3d(sQ + t * L::kTileBytes + ch * L::kChunk, &mq, ch * 64, qb * kTile, it.bh,
-                        bar.q_full(t));
+            tma_load_3d(sQ + ch * L::kChunk, &mq, ch * 64, it.r * kTile, it.bh, bar.q_full());
+          for (int j = 0; ok && j < it.ntiles; ++j, ++J)
+            ok = load_k(J, it.list[j] >> 2, it.bh);
+          J_last = J - 1;
         }
-        for (int j = 0; ok && j < it.count; ++j, ++J) {
-          const int slot = J % KS;
-          if (J >= KS && !mbar_wait(bar.k_empty(slot), ((J / KS) - 1) & 1, p.status)) {
-            record_failure(p.status, kStatusTimeout, kSiteFwdKEmpty);
-            ok = false;
-            break;
-          }
-          const int kb = it.list[j] >> 4;
-          mbar_arrive_expect_tx(bar.k_full(slot), L::kTileBytes);
-          for (int ch = 0; ch < L::kChunks; ++ch)
-            tma_load_3d(sK + slot * L::kTileBytes + ch * L::kChunk, &mk, ch * 64, kb * kTile,
-                        it.bh, bar.k_full(slot));
-        }
-        if (!ok) break;
         // claim the next item once this one's loads are issued; its ring
         // entry was last used by item k - 1, which every reader has taken
         const int nxt = claim();
         const int s = (k + 1) & 1;
         if (k >= 1 && !mbar_wait(bar.sched_empty(s), ((k - 1) >> 1) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteFwdSched);
+          ok = false;
           break;
         }
         sched[s] = nxt;
@@ -301,34 +323,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = read_item(k, ok);
         if (n < 0) break;
         const Item it = decode(n);
-        for (int j = 0; ok && j < it.count; ++j, ++J) {
-          const int slot = J % VS;
-          if (J >= VS && !mbar_wait(bar.v_empty(slot), ((J / VS) - 1) & 1, p.status)) {
+        for (int j = 0; ok && j < it.ntiles; ++j, ++J) {
+          const int slot = J % kVSlots;
+          if (J >= kVSlots &&
+              !mbar_wait(bar.pv_done(slot), ((J / kVSlots) - 1) & 1, p.status)) {
             record_failure(p.status, kStatusTimeout, kSiteFwdVEmpty);
             ok = false;
             break;
           }
-          const int kb = it.list[j] >> 4;
           mbar_arrive_expect_tx(bar.v_full(slot), L::kTileBytes);
           if constexpr (kFp8) {
             // V^T tile: the head's 128 rows of d, the block's 128 keys
-            tma_load_2d(sV + slot * L::kTileBytes, &mv, kb * kTile, it.bh * 128, bar.v_full(slot));
+            tma_load_2d(sV + slot * L::kTileBytes, &mv, (it.list[j] >> 2) * kTile, it.bh * 128,
+                        bar.v_full(slot));
           } else {
             for (int ch = 0; ch < L::kChunks; ++ch)
-              tma_load_3d(sV + slot * L::kTileBytes + ch * L::kChunk, &mv, ch * 64, kb * kTile,
-                          it.bh, bar.v_full(slot));
+              tma_load_3d(sV + slot * L::kTileBytes + ch * L::kChunk, &mv, ch * 64,
+                          (it.list[j] >> 2) * kTile, it.bh, bar.v_full(slot));
           }
         }
       }
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer (both tiles)
-    // One thread issues every product in the order, per step j of the merged
-    // list, S_0(j), O_1 += P_1 V (previous step of tile 1), S_1(j),
-    // O_0 += P_0 V (step j): while one tile's softmax runs, the tensor pipe
-    // holds the other tile's products, so the two softmax warpgroups
-    // alternate. S_t(j) overwrites the TMEM columns the previous P_t V read, so
-    // it waits for that product to complete.
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = kFp8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, 0, 1);
@@ -336,176 +353,156 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kPvSteps = kFp8 ? 4 : 8;           // K steps (keys) of O += P V
       // Shared-memory descriptors are built once: the address field (bits
       // 0-13, in 16-byte units) of every operand stays below 2^14 here, so a
-      // descriptor for base + off is the base descriptor plus off / 16.
-      const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
-      const uint64_t dq1 = sdesc_sw128(sQ + L::kTileBytes, 16, 1024);
+      // descriptor for base + off is the base descriptor plus off / 16. This
+      // keeps the per-MMA instruction stream of this thread short.
+      const uint64_t dq_base = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk_base = sdesc_sw128(sK, 16, 1024);
       // V is MN-major [keys][d] in bf16, K-major [d][keys] as e4m3 V^T
       const uint64_t dv_base = kFp8 ? sdesc_sw128(sV, 16, 1024) : sdesc_sw128(sV, 16384, 1024);
-      bool ok = true;
-      int J0 = 0;                // running step of the item's first entry
-      int nv[2] = {0, 0};        // P V products per tile so far
-      // S_t of step J into TMEM (K of step J has landed); the previous P_t V
-      // must have completed
-      auto issue_s = [&](int t, int J) -> bool {
-        if (nv[t] > 0 && !mbar_wait(bar.pv_done(t), (nv[t] - 1) & 1, p.status)) return false;
-        tc_fence_after();
-        const uint64_t dq = t == 0 ? dq0 : dq1;
-        const uint64_t kd = dk_base + static_cast<uint64_t>(((J % KS) * L::kTileBytes) >> 4);
-        const uint32_t ts = tmem + col_s(t);
-#pragma unroll
-        for (int kk = 0; kk < kSSteps; ++kk) {
-          // 32 bytes of each 128-byte row per K step (16 bf16 or 32 e4m3)
-          const uint64_t off16 = static_cast<uint64_t>(((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4);
-          if constexpr (kFp8)
-            mma_ss_f8(ts, dq + off16, kd + off16, idesc_s, kk > 0);
-          else
-            mma_ss(ts, dq + off16, kd + off16, idesc_s, kk > 0);
-        }
-        mma_commit(bar.s_full(t));
-        return true;
-      };
-      // O_t += P_t V of step J once P_t is in TMEM and V has landed; the item's
-      // first product overwrites O_t after the previous item's O_t was read out
-      auto issue_pv = [&](int t, int J, bool first, int k) -> bool {
-        const int vs = J % VS;
-        if (!mbar_wait(bar.p_full(t), nv[t] & 1, p.status) ||
-            !mbar_wait(bar.v_full(vs), (J / VS) & 1, p.status) ||
-            (first && k > 0 && !mbar_wait(bar.o_free(t), (k - 1) & 1, p.status)))
+      // S of step J into region J % 3 once K_J has landed and O += P V of
+      // step J - 3 (the last reader of that region) has completed
+      auto issue_s = [&](int J) -> bool {
+        const int slot = J % kKSlots, g = J % kSRegions;
+        if (J >= kSRegions &&
+            !mbar_wait(bar.pv_done(g), ((J / kSRegions) - 1) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdO);
           return false;
-        tc_fence_after();
-        const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
-        const uint32_t ts = tmem + col_s(t), to = tmem + col_o(t);
-#pragma unroll
-        for (int kk = 0; kk < kPvSteps; ++kk) {
-          // A: P, 8 TMEM columns per K step; B: the next 16 key rows of V
-          // (bf16) or the next 32 key bytes of each row of V^T (e4m3)
-          if constexpr (kFp8)
-            mma_ts_f8(to, ts + 8 * kk, vd + static_cast<uint64_t>((kk * 32) >> 4), idesc_pv,
-                      (!first || kk > 0));
-          else
-            mma_ts(to, ts + 8 * kk, vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv,
-                   (!first || kk > 0));
         }
-        mma_commit(bar.pv_done(t));
-        ++nv[t];
+        if (!mbar_wait(bar.k_full(slot), (J / kKSlots) & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdK);
+          return false;
+        }
+        tc_fence_after();
+        const uint64_t kd = dk_base + static_cast<uint64_t>((slot * L::kTileBytes) >> 4);
+#pragma unroll
+        for (int k = 0; k < kSSteps; ++k) {
+          // 32 bytes of each 128-byte row per K step (16 bf16 or 32 e4m3)
+          const uint64_t off16 = static_cast<uint64_t>(((k >> 2) * L::kChunk + (k & 3) * 32) >> 4);
+          if constexpr (kFp8)
+            mma_ss_f8(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, k > 0);
+          else
+            mma_ss(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, k > 0);
+        }
+        mma_commit(bar.s_full(g));  // also frees K slot J % 3
         return true;
       };
+      bool ok = true;
+      int J = 0, ti = 0;  // running step; items with tiles so far
       for (int k = 0; ok; ++k) {
         const int n = read_item(k, ok);
         if (n < 0) break;
-        const Item it = decode(n);
-        if (!mbar_wait(bar.q_full(0), k & 1, p.status) ||
-            !mbar_wait(bar.q_full(1), k & 1, p.status)) {
-          ok = false;
+        const int ntiles = decode(n).ntiles;
+        if (ntiles == 0) continue;
+        if (!mbar_wait(bar.q_full(), ti & 1, p.status)) {
+          record_failure(p.status, kStatusTimeout, kSiteFwdQ);
           break;
         }
-        // the last step each tile visits: Q_t is free for the next item once
-        // that step's S_t has completed (usually found at once: the list's
-        // last entry, or the one before it)
-        int last[2];
-        for (int t = 0; t < 2; ++t) {
-          last[t] = it.count - 1;
-          while (last[t] >= 0 && label(it.list[last[t]], t) == FM_TILE_FULL) --last[t];
-          if (last[t] < 0) mma_commit(bar.q_empty(t));
+        tc_fence_after();
+        // S runs three steps ahead of O += P V: the item's first three now,
+        // then S_{J+3} right after O += P_J V_J (same region) has completed,
+        // which keeps S off the softmax -> P V chain
+        for (int m = 0; ok && m < kSRegions && m < ntiles; ++m) ok = issue_s(J + m);
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int Jj = J + j, g = Jj % kSRegions, vs = Jj % kVSlots;
+          if (!mbar_wait(bar.go(g), (Jj / kSRegions) & 1, p.status)) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdP);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kPvSteps; ++kk) {
+            // A: P, 8 TMEM columns per K step; B: the next 16 key rows of V
+            // (bf16) or the next 32 key bytes of each row of V^T (e4m3)
+            if constexpr (kFp8)
+              mma_ts_f8(tmem + kColO, tmem + 128 * g + 8 * kk,
+                        vd + static_cast<uint64_t>((kk * 32) >> 4), idesc_pv, (j > 0 || kk > 0));
+            else
+              mma_ts(tmem + kColO, tmem + 128 * g + 8 * kk,
+                     vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (j > 0 || kk > 0));
+          }
+          mma_commit(bar.pv_done(g));  // also frees V slot J % 3
+          if (j + kSRegions < ntiles) ok = issue_s(Jj + kSRegions);
         }
-        bool first[2] = {true, true};
-        int pend1 = -1;  // step of tile 1 whose P V is still to be issued
-        for (int j = 0; ok && j < it.count; ++j) {
-          const int J = J0 + j, entry = it.list[j];
-          const bool a0 = label(entry, 0) != FM_TILE_FULL, a1 = label(entry, 1) != FM_TILE_FULL;
-          ok = mbar_wait(bar.k_full(J % KS), (J / KS) & 1, p.status);
-          if (ok && a0) {
-            ok = issue_s(0, J);
-            if (ok && j == last[0]) mma_commit(bar.q_empty(0));
-          }
-          if (ok && pend1 >= 0) {
-            // tile 1's previous step: its V slot is released after this product
-            ok = issue_pv(1, pend1, first[1], k);
-            if (ok) mma_commit(bar.v_empty(pend1 % VS));
-            first[1] = false;
-            pend1 = -1;
-          }
-          if (ok && a1) {
-            ok = issue_s(1, J);
-            if (ok && j == last[1]) mma_commit(bar.q_empty(1));
-            pend1 = J;
-          }
-          if (ok) mma_commit(bar.k_empty(J % KS));  // both tiles' S of this step issued
-          if (ok && a0) {
-            ok = issue_pv(0, J, first[0], k);
-            first[0] = false;
-          }
-          // V of this step is released now unless tile 1 still needs it
-          if (ok && !a1) {
-            ok = mbar_wait(bar.v_full(J % VS), (J / VS) & 1, p.status);
-            if (ok) mma_commit(bar.v_empty(J % VS));
-          }
-        }
-        if (ok && pend1 >= 0) {
-          ok = issue_pv(1, pend1, first[1], k);
-          if (ok) mma_commit(bar.v_empty(pend1 % VS));
-        }
-        if (!ok) {
-          record_failure(p.status, kStatusTimeout, kSiteFwdP);
-          break;
-        }
-        J0 += it.count;
+        J += ntiles;
+        ++ti;
       }
     }
-  }
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ gatekeeper
+    if (lane == 0) {
+      bool ok = true;
+      int J = 0, ti = 0;
+      for (int k = 0; ok; ++k) {
+        const int n = read_item(k, ok);
+        if (n < 0) break;
+        const int ntiles = decode(n).ntiles;
+        if (ntiles == 0) continue;
+        for (int j = 0; j < ntiles; ++j, ++J) {
+          const int g = J % kSRegions;
+          ok = mbar_wait(bar.v_full(J % kVSlots), (J / kVSlots) & 1, p.status);
+          // the item's first O += P V overwrites O: the previous item's O must
+          // have been read out
+          if (j == 0 && ti > 0) ok = ok && mbar_wait(bar.o_free(), (ti - 1) & 1, p.status);
+          ok = ok && mbar_wait(bar.p_full(g), (J / kSRegions) & 1, p.status);
+          if (!ok) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdP);
+            break;
+          }
+          mbar_arrive(bar.go(g));
+        }
+        ++ti;
+      }
+    }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax) : "memory");
-    // ------------------------------------------------------------ softmax of tile t
-    const int t = warp >> 2;
+    // ------------------------------------------------------------ softmax
+    const int w = warp >> 2;                 // warpgroup: key columns [64w, 64w+64)
     const int row = (warp & 3) * 32 + lane;  // query row within the block = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t ts = tmem + lane_base + col_s(t), to = tmem + lane_base + col_o(t);
     constexpr float kThresh = kFp8 ? kRescaleThresholdFp8 : kRescaleThreshold;
-    volatile int* share = sched + 2 + 2 * t;
     // After a failed wait the warp keeps stepping through its items without
-    // touching TMEM, so that the four warps pass the same named barriers and
+    // touching TMEM, so that all eight warps pass the same named barriers and
     // the CTA can still reach its exit; `ok` is kept uniform across the warp.
     bool ok = true;
-    int ns = 0;  // products of this tile so far
+    int J = 0;  // running step
     for (int k = 0;; ++k) {
-      if ((warp & 3) == 0 && lane == 0) {
+      // warp 0 takes the item from the ring and shares it through shared
+      // memory, so that the eight warps agree on it even after a failure
+      if (warp == 0 && lane == 0) {
         bool okr = true;
-        share[k & 1] = read_item(k, okr);
+        sched[2 + (k & 1)] = read_item(k, okr);
       }
-      group_bar(t);
-      const int n = share[k & 1];
+      softmax_bar();
+      const int n = sched[2 + (k & 1)];
       if (n < 0) break;
       const Item it = decode(n);
-      const int r = t == 0 ? it.r0 : it.r1;
-      const bool tile_exists = r < p.Tr;
-      const int bh = it.bh, bm = it.bm;
+      const int ntiles = it.ntiles, r = it.r, bh = it.bh, bm = it.bm;
       // FP8: the true score is S times scale_Q(query block) * scale_K(key
       // block); the product folds into each tile's exponent scale c
-      const float c_row = (kFp8 && tile_exists)
-                              ? p.scale_log2 * p.qscale[static_cast<size_t>(bh) * p.Tr + r]
-                              : p.scale_log2;
+      const float c_row = kFp8 ? p.scale_log2 * p.qscale[static_cast<size_t>(bh) * p.Tr + r]
+                               : p.scale_log2;
       float m = -INFINITY, l = 0.f;
-      bool first = true;  // no product of this tile in the item yet
-      for (int j = 0; j < it.count; ++j) {
-        const int entry = it.list[j];
-        const int lab = label(entry, t);
-        if (lab == FM_TILE_FULL) continue;
-        const int kb = entry >> 4;
+      int next_entry = ntiles > 0 ? it.list[0] : 0;  // read one step ahead
+      for (int j = 0; j < ntiles; ++j) {
+        const int Jj = J + j;
+        const int entry = next_entry;
+        if (j + 1 < ntiles) next_entry = it.list[j + 1];
+        const int g = Jj % kSRegions;
         const float c =
-            kFp8 ? c_row * p.kscale[static_cast<size_t>(bh) * p.Tc + kb] : c_row;
+            kFp8 ? c_row * p.kscale[static_cast<size_t>(bh) * p.Tc + (entry >> 2)] : c_row;
         // The element mask applies on PARTIAL tiles and on every tile of a short
         // last key block (its keys >= N do not exist and are masked).
-        const bool short_keys = kShortLast && kb == p.Tc - 1;
-        const bool partial = lab == FM_TILE_PARTIAL || short_keys;
-        // lane l builds the masked-row bits of key column 32q + l for this
+        const bool short_keys = kShortLast && (entry >> 2) == p.Tc - 1;
+        const bool partial = (entry & 3) == FM_TILE_PARTIAL || short_keys;
+        // lane l builds the masked-row bits of key column 64w + 32k + l for this
         // warp's 32 rows; a bit transpose hands each lane its own row's bits
         // over those 32 columns. The bound loads overlap the wait for S.
-        uint32_t mbits[4] = {0u, 0u, 0u, 0u};
+        uint32_t mbits[2] = {0u, 0u};
         if (partial) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int jc = kb * kTile + 32 * q + lane;
+          for (int kk = 0; kk < 2; ++kk) {
+            const int jc = (entry >> 2) * kTile + 64 * w + 32 * kk + lane;
             uint32_t colbits = 0xffffffffu;  // a key >= N masks every row
             if (!kShortLast || jc < p.N) {
               const size_t col = static_cast<size_t>(bm) * p.N + jc;
@@ -515,35 +512,43 @@ __global__ void __launch_bounds__(kThreads, 1)
               colbits = column_mask_bits(jc, lts, lte, uts, ute, p.mask.causal != 0,
                                          r * kTile + 32 * (warp & 3));
             }
-            mbits[q] = warp_transpose_bits(colbits);
+            mbits[kk] = warp_transpose_bits(colbits);
           }
         }
         if (ok) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar.s_full(t), ns & 1, p.status));
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar.s_full(g), (Jj / kSRegions) & 1, p.status));
           if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdS);
         }
+        uint32_t sv[64];
+        float pm = -INFINITY;
         if (ok) {
           tc_fence_after();
-          uint32_t sv[128];
-          tmem_ld64(ts, ts + 32, *reinterpret_cast<uint32_t(*)[64]>(sv));
-          tmem_ld64(ts + 64, ts + 96, *reinterpret_cast<uint32_t(*)[64]>(sv + 64));
+          const uint32_t s_addr = tmem + lane_base + 128 * g + 64 * w;
+          tmem_ld64(s_addr, s_addr + 32, sv);
           if (partial) {
 #pragma unroll
-            for (int jj = 0; jj < 128; ++jj)
+            for (int jj = 0; jj < 64; ++jj)
               sv[jj] = ((mbits[jj >> 5] >> (jj & 31)) & 1u) ? 0xff800000u : sv[jj];
           }
-          float mx[8];
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(sv[u]);
-#pragma unroll
-          for (int jj = 8; jj < 128; jj += 8) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(sv[jj + u]));
+          for (int jj = 0; jj < 64; jj += 4) {
+            mx0 = fmaxf(mx0, __uint_as_float(sv[jj]));
+            mx1 = fmaxf(mx1, __uint_as_float(sv[jj + 1]));
+            mx2 = fmaxf(mx2, __uint_as_float(sv[jj + 2]));
+            mx3 = fmaxf(mx3, __uint_as_float(sv[jj + 3]));
           }
-          const float pm =
-              fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * c;
-          const float m_new = fmaxf(m, pm);
+          pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+        }
+        // exchange the two partial row maxima (double-buffered by step parity);
+        // the barrier also orders both warpgroups' S loads before any P store
+        // into the region
+        red[((Jj & 1) * 2 + w) * kTile + row] = pm;
+        softmax_bar();
+        if (ok) {
+          const float mx = fmaxf(pm, red[((Jj & 1) * 2 + (w ^ 1)) * kTile + row]);
+          const float m_new = fmaxf(m, mx);
           const bool rescale = m_new > m + kThresh;
           float alpha = 1.f;
           if (rescale) {
@@ -552,82 +557,101 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float m_use = (m == -INFINITY) ? 0.f : m;
           // pairs of columns through the paired fp32 instructions: s * c - m
-          // and the running pairs of partial sums take one issue slot per pair
+          // and the running pair of partial sums take one issue slot per pair
           const uint64_t c2 = f2_make(c, c), nm2 = f2_make(-m_use, -m_use);
-          uint64_t la = f2_make(0.f, 0.f), lb = f2_make(0.f, 0.f);
-          // P is packed in place over the S registers already consumed: bf16
-          // pairs in sv[0..63], or e4m3 quads in sv[0..31]
+          uint64_t l2 = f2_make(0.f, 0.f);
+          uint32_t pk[32];  // bf16 pairs; FP8: e4m3 quads in pk[0..15]
           float pq0 = 0.f, pq1 = 0.f;
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
+          for (int i = 0; i < 32; ++i) {
             float x0, x1;
             f2_split(f2_fma(f2_make(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
                             c2, nm2),
                      x0, x1);
             const float p0 = ex2(x0), p1 = ex2(x1);
-            if (i & 1)
-              lb = f2_add(lb, f2_make(p0, p1));
-            else
-              la = f2_add(la, f2_make(p0, p1));
+            l2 = f2_add(l2, f2_make(p0, p1));
             if constexpr (kFp8) {
               // the scale keeps small probabilities above e4m3's subnormal range
               if (i & 1)
-                sv[i >> 1] = pack_e4m3x4(pq0, pq1, p0 * kFp8PScale, p1 * kFp8PScale);
+                pk[i >> 1] = pack_e4m3x4(pq0, pq1, p0 * kFp8PScale, p1 * kFp8PScale);
               else
                 pq0 = p0 * kFp8PScale, pq1 = p1 * kFp8PScale;
             } else {
-              sv[i] = pack_bf16x2(p0, p1);
+              pk[i] = pack_bf16x2(p0, p1);
             }
           }
-          float l0, l1, l2, l3;
-          f2_split(la, l0, l1);
-          f2_split(lb, l2, l3);
-          l = l * alpha + ((l0 + l1) + (l2 + l3));
-          // P over S_t's own columns: keys [0, 128) as bf16 pairs in columns
-          // [0, 64) (the A operand of P V), or as e4m3 quads in columns [0, 32)
-          tmem_st32p(ts, sv);
-          if constexpr (!kFp8) tmem_st32p(ts + 32, sv + 32);
-          // O_t is quiescent here (its last product completed before S_t was
-          // issued); the item's first product overwrites it, so no rescale then
-          if (!first && __any_sync(0xffffffffu, rescale)) {
+          float l0, l1;
+          f2_split(l2, l0, l1);
+          l = l * alpha + (l0 + l1);
+          // P_j over this warpgroup's part of S_j's region: keys [64w, 64w+64)
+          // as bf16 pairs in columns [32w, 32w+32) (the A operand of P V)
+          if constexpr (kFp8) {
+            // ... or as e4m3 quads in columns [16w, 16w+16)
+            tmem_st16(tmem + lane_base + 128 * g + 16 * w,
+                      *reinterpret_cast<const uint32_t(*)[16]>(pk));
+          } else {
+            tmem_st32p(tmem + lane_base + 128 * g + 32 * w, pk);
+          }
+          if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+            // O is rescaled once O += P_{j-1} V_{j-1} has completed
+            ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done((Jj - 1) % kSRegions),
+                                                   ((Jj - 1) / kSRegions) & 1, p.status));
+            if (ok) {
+              tc_fence_after();
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) tmem_scale32(to + 32 * ch, alpha);
+              for (int ch = 0; ch < kOCols / 32; ++ch)
+                tmem_scale_cols<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, alpha);
+            } else if (lane == 0) {
+              record_failure(p.status, kStatusTimeout, kSiteFwdO);
+            }
           }
           tmem_st_wait();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar.p_full(t));
-        first = false;
-        ++ns;
+        if (lane == 0) mbar_arrive(bar.p_full(g));
       }
       // ---------------------------------------------------------- epilogue of the item
-      const bool live = ok && !first;
-      if (live) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(t), (ns - 1) & 1, p.status));
+      if (ok && ntiles > 0) {
+        const int jl = J + ntiles - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(jl % kSRegions),
+                                               (jl / kSRegions) & 1, p.status));
         if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdO);
         tc_fence_after();
       }
-      const bool has = live && ok && l > 0.f;
+      // row sums through the exchange buffer of the parity the item's last
+      // step did not use (its readers passed that step's barrier)
+      float* lsum = red + ((J + ntiles) & 1) * 2 * kTile;
+      lsum[w * kTile + row] = l;
+      softmax_bar();
+      const float ltot = l + lsum[(w ^ 1) * kTile + row];
+      const bool live = ok && ntiles > 0;
+      const bool has = live && ltot > 0.f;
       // FP8: O accumulated (kFp8PScale P) (V / scale_V)
-      const float inv = has ? (kFp8 ? p.vscale[bh] * (1.f / kFp8PScale) : 1.f) / l : 0.f;
-      // rows >= N of a short last query block, and a missing second block, do
-      // not exist: nothing is stored for them
-      const bool row_exists = tile_exists && (!kShortLast || r * kTile + row < p.N);
-      const size_t orow0 = static_cast<size_t>(bh) * p.N + static_cast<size_t>(r) * kTile + row;
-      uint16_t* orow = p.o + (row_exists ? orow0 : 0) * D;
+      const float inv = has ? (kFp8 ? p.vscale[bh] * (1.f / kFp8PScale) : 1.f) / ltot : 0.f;
+      // rows >= N of a short last query block do not exist: nothing is stored
+      const bool row_exists = !kShortLast || r * kTile + row < p.N;
+      uint16_t* orow = p.o + static_cast<size_t>(it.q_row0 + row) * D + w * kOCols;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch)
-        tmem_cols_to_bf16(to + 32 * ch, live && ok, inv, orow + 32 * ch, row_exists);
-      // O_t has been read (the loads above completed): the next item's first
-      // product may overwrite it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.o_free(t));
-      if (row_exists) {
-        const float m_fin = (m == -INFINITY) ? 0.f : m;
-        p.lse[orow0] = has ? (m_fin + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      for (int ch = 0; ch < kOCols / 32; ++ch)
+        tmem_cols_to_bf16<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, live, inv,
+                              orow + 32 * ch, row_exists);
+      if (ntiles > 0) {
+        // O has been read (the loads above completed): the next item's first
+        // O += P V may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.o_free());
       }
+      if (w == 0 && row_exists) {
+        const float m_fin = (m == -INFINITY) ? 0.f : m;
+        p.lse[it.q_row0 + row] =
+            has ? (m_fin + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
+      }
+      J += ntiles;
+      // every warp has read lsum before the next item's first step (or
+      // epilogue) writes the same buffer
+      softmax_bar();
     }
   }
 
@@ -646,15 +670,9 @@ cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kShortLast, kFp8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  // the register split inside the kernel needs the full pool at launch; a
-  // build that allocated fewer registers per thread is refused, not run
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, fwd_kernel<D, kShortLast, kFp8>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs * kThreads < kRegPool) return cudaErrorInvalidConfiguration;
   // persistent: one CTA per SM (at most one per work item); the item counter
   // starts at zero
-  const int items = p.B * p.H * p.Tp;
+  const int items = p.B * p.H * p.Tr;
   const unsigned grid = static_cast<unsigned>(items < p.num_sms ? items : p.num_sms);
   e = cudaMemsetAsync(p.sched, 0, sizeof(int32_t), s);
   if (e != cudaSuccess) return e;

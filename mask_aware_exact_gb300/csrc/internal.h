@@ -40,13 +40,6 @@ struct ClassifyTables {
   int32_t* col_count;  // [B,Hm,Tc]
   int32_t* col_list;   // [B,Hm,Tc,Tr]
   int32_t* col_order;  // [B,Hm,Tc]
-  // Pairs of query blocks (2p, 2p + 1), Tp = ceil(Tr / 2): the merged
-  // ascending list of key blocks that are non-FULL for either block, each entry
-  // (key block << 4) | (label of block 2p << 2) | label of block 2p + 1, with
-  // FM_TILE_FULL standing for "not visited" (and for a block 2p + 1 >= Tr).
-  int32_t* pair_count;  // [B,Hm,Tp]
-  int32_t* pair_list;   // [B,Hm,Tp,Tc]
-  int32_t* pair_order;  // [B,Hm,Tp]
 };
 
 // FP8 operands of the FP8 forward (in the workspace): Q and K e4m3 [B*H, N, 128]
@@ -69,10 +62,9 @@ struct FwdParams {
   const float* qscale;  // FP8 forward only: per-block scales of Q, K and per-head scale of V
   const float* kscale;
   const float* vscale;
-  int Tp;  // query-block pairs per head
-  const int32_t* pair_count;
-  const int32_t* pair_list;
-  const int32_t* pair_order;
+  const int32_t* row_count;
+  const int32_t* row_list;
+  const int32_t* row_order;
   uint16_t* o;  // bf16 [B,H,N,d]
   float* lse;   // [B,H,N]
   int32_t* status;

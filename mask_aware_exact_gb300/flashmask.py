@@ -33,8 +33,7 @@ class _FmMask(ctypes.Structure):
 class FmWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "minmax", "labels", "labels_t", "row_count", "row_list", "row_order",
-                 "col_count", "col_list", "col_order", "pair_count", "pair_list", "pair_order",
-                 "lse2", "delta", "dq_accum", "total")]
+                 "col_count", "col_list", "col_order", "lse2", "delta", "dq_accum", "total")]
 
 
 class FmFp8Layout(ctypes.Structure):
@@ -321,7 +320,6 @@ def read_classification(ws: torch.Tensor, B: int, Hm: int, N: int) -> dict:
     """Copies the classification regions of a workspace to host numpy arrays."""
     L = flashmask_workspace_layout(B, Hm, Hm, N, 64, False)
     Tr = Tc = (N + FM_TILE - 1) // FM_TILE
-    Tp = (Tr + 1) // 2
     h = ws[:L.total].cpu().numpy()
 
     def region(off, count, dtype, shape):
@@ -337,9 +335,6 @@ def read_classification(ws: torch.Tensor, B: int, Hm: int, N: int) -> dict:
         "col_count": region(L.col_count, B * Hm * Tc, np.int32, (B, Hm, Tc)),
         "col_list": region(L.col_list, B * Hm * Tc * Tr, np.int32, (B, Hm, Tc, Tr)),
         "col_order": region(L.col_order, B * Hm * Tc, np.int32, (B, Hm, Tc)),
-        "pair_count": region(L.pair_count, B * Hm * Tp, np.int32, (B, Hm, Tp)),
-        "pair_list": region(L.pair_list, B * Hm * Tp * Tc, np.int32, (B, Hm, Tp, Tc)),
-        "pair_order": region(L.pair_order, B * Hm * Tp, np.int32, (B, Hm, Tp)),
     }
 
 

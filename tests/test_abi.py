@@ -52,9 +52,6 @@ def test_workspace_sizes(lib):
         assert fm.flashmask_workspace_bytes(*bad, True) == 0
     # the longest supported sequence (FM_MAX_SEQLEN = 2^21) is accepted
     assert fm.flashmask_workspace_bytes(1, 1, 1, 1 << 21, 64, False) > 0
-    # the pair tables of the forward: ceil(Tr / 2) pairs of query blocks
-    L = fm.flashmask_workspace_layout(1, 2, 1, 1000, 64, True)
-    assert L.pair_list - L.pair_count >= 4 * 4 and L.pair_order - L.pair_list >= 4 * 8 * 4
     # a sequence length that is not a multiple of 128: the tables cover
     # ceil(N / 128) blocks and the backward arrays are padded to 128 rows
     L = fm.flashmask_workspace_layout(1, 2, 1, 1000, 64, True)
@@ -65,8 +62,7 @@ def test_workspace_sizes(lib):
 def test_workspace_layout_regions_disjoint(lib):
     L = fm.flashmask_workspace_layout(2, 8, 2, 1024, 64, True)
     offs = [L.status, L.minmax, L.labels, L.labels_t, L.row_count, L.row_list, L.row_order,
-            L.col_count, L.col_list, L.col_order, L.pair_count, L.pair_list, L.pair_order,
-            L.lse2, L.delta, L.dq_accum, L.total]
+            L.col_count, L.col_list, L.col_order, L.lse2, L.delta, L.dq_accum, L.total]
     assert offs == sorted(offs) and len(set(offs)) == len(offs)
     assert all(o % 256 == 0 for o in offs)
     Tr = 1024 // 128

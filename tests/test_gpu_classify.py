@@ -37,20 +37,7 @@ def check_consistency(c, b, hm):
         assert n == len(keep)
         lst = c["col_list"][b, hm, cc, :n]
         assert np.array_equal(lst >> 2, keep) and np.array_equal(lst & 3, lab[keep, cc])
-    # pairs of query blocks (2p, 2p + 1): merged ascending lists carrying both
-    # labels, FULL marking a block not visited (and a missing block 2p + 1)
-    Tp = (Tr + 1) // 2
-    for pr in range(Tp):
-        a = lab[2 * pr]
-        bb = lab[2 * pr + 1] if 2 * pr + 1 < Tr else np.full(Tc, TL.TILE_FULL, np.uint8)
-        keep = np.nonzero((a != TL.TILE_FULL) | (bb != TL.TILE_FULL))[0]
-        n = c["pair_count"][b, hm, pr]
-        assert n == len(keep)
-        lst = c["pair_list"][b, hm, pr, :n]
-        assert np.array_equal(lst >> 4, keep)
-        assert np.array_equal((lst >> 2) & 3, a[keep]) and np.array_equal(lst & 3, bb[keep])
-    for key, cnt in (("row_order", c["row_count"][b, hm]), ("col_order", c["col_count"][b, hm]),
-                     ("pair_order", c["pair_count"][b, hm])):
+    for key, cnt in (("row_order", c["row_count"][b, hm]), ("col_order", c["col_count"][b, hm])):
         order = c[key][b, hm]
         assert sorted(order.tolist()) == list(range(len(order)))  # a permutation
         assert np.all(np.diff(cnt[order]) <= 0)                  # longest first
