@@ -114,11 +114,6 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 __device__ __forceinline__ void drain_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-// Fire-and-forget fp32 add into global memory (performed in L2).
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
 
 // ---------------------------------------------------------------- preprocess
 // One padded row (bh, n) per D/8 threads, n < Npad: rows n >= N (the short last
@@ -173,10 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                const __grid_constant__ CUtensorMap mdq, const BwdParams p) {
   using L = BwdLayout<D>;
-  // d = 128: dQ_t is computed transposed and reduced into the accumulator
-  // straight from registers; d = 64 stages it through the tile's stage
-  // buffers and adds it with a TMA bulk reduction
-  constexpr bool kDirectDq = D == 128;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -336,29 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           record_failure(p.status, kStatusTimeout, kSiteBwdDS);
           break;
         }
-        // d = 128 (the dQ tile does not pass through the stage buffers): the
-        // compute warps are done with this stage's D values, and the dO buffer
-        // is free once dP^T and dV have completed
-        if constexpr (kDirectDq) mma_commit(bar.do_empty(st));
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t off = d16((k >> 2) * 16384 + (k & 3) * 32);
           mma_ss(tmem + kColDK, kDS + off, mQ + stage + d16(k * 2048), id_kd, (t > 0 || k > 0));
         }
-        if constexpr (kDirectDq) {
-          mma_commit(bar.q_empty(st));  // Q read by S^T and dK
-          // dQ_t^T = K^T dS^T: A = K read MN-major (M = d), B = dS^T read
-          // MN-major (N = queries); TMEM lanes = d, columns = queries
+        // dQ_t = dS K: A = dS^T read MN-major (M = queries), B = K read MN-major
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + kColDP, mK + d16(k * 2048), mDS + d16(k * 2048), id_dq, k > 0);
-        } else {
-          // dQ_t = dS K: A = dS^T read MN-major (M = queries), B = K read MN-major
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + kColDP, mDS + d16(k * 2048), mK + d16(k * 2048), id_dq, k > 0);
-        }
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + kColDP, mDS + d16(k * 2048), mK + d16(k * 2048), id_dq, k > 0);
         mma_commit(bar.tile_done());
       }
     }
@@ -513,36 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every lane takes part in the (warp-collective) TMEM load; only
         // existing keys store
         if (key_exists) store_row32_bf16(dst_row + ch * 32, v, f);
-      }
-    }
-  } else if constexpr (kDirectDq) {
-    // ------------------------------------------------------------ dQ drain (d = 128)
-    // thread = TMEM lane = head-dimension index c; each 32-column TMEM load
-    // gives 32 queries of that column, and a warp's reductions for one query
-    // cover 32 consecutive fp32 of the accumulator row (one 128-byte line)
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int c = (warp & 3) * 32 + lane;
-    for (int t = 0; t < ntiles; ++t) {
-      const int qb = list[t] >> 2;
-      if (!mbar_wait(bar.tile_done(), t & 1, p.status)) {
-        record_failure(p.status, kStatusTimeout, kSiteBwdDQ);
-        break;
-      }
-      tc_fence_after();
-      float* acc = p.dq_accum + (static_cast<size_t>(bh) * p.Npad + qb * kTile) * D + c;
-#pragma unroll
-      for (int ch = 0; ch < kTile / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kColDP + ch * 32, v);
-        if (ch == kTile / 32 - 1) {
-          // the dQ columns have been read: the next tile's dP^T may overwrite them
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar.dq_drained());
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          red_add_f32(acc + static_cast<size_t>(ch * 32 + i) * D, __uint_as_float(v[i]));
       }
     }
   } else {
