@@ -307,3 +307,29 @@ def test_forwards_on_two_streams_with_their_own_workspaces():
     for i in range(2):
         o_ref, lse_ref = A.forward(*inputs[i], specs[i], 1 / math.sqrt(d))
         check_forward(to_np(seq[i][0]), to_np(seq[i][1]), o_ref, lse_ref, f"forward {i}")
+
+
+@pytest.mark.parametrize("N,d", [(200, 128), (77, 64)])
+def test_ragged_tail_ignores_neighbouring_head(N, d):
+    # The short last block of a head is padded by the TMA loads: rows past the
+    # head's end read zeros, never the next head's rows. So a neighbouring head
+    # full of Inf / NaN must leave this head's outputs and gradients exact
+    # (P = 0 on missing keys would still give 0 * Inf = NaN otherwise).
+    fm = need_gpu()
+    B, H = 1, 3
+    spec = W.document_bounds(B, 1, [N // 2, N - N // 2])
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=N + 5)
+    bad = [x.clone() for x in (q, k, v, do)]
+    for x in bad:
+        x[0, 1] = float("inf")
+        x[0, 1, ::3] = float("nan")
+    out = run_path(fm, *bad, spec)
+    scale = 1 / math.sqrt(d)
+    lts, lte, uts, ute = head_bounds(spec, 0, 0, H)
+    for h in (0, 2):  # the finite heads on either side of the poisoned one
+        o_ref, lse_ref = A.forward_head(q[0, h], k[0, h], v[0, h], lts, lte, uts, ute, True, scale)
+        check_forward(to_np(out["o"][0, h]), to_np(out["lse"][0, h]), o_ref, lse_ref, f"head {h}")
+        g_ref = A.backward_head(q[0, h], k[0, h], v[0, h], do[0, h], lts, lte, uts, ute, True, scale)
+        for name, g, r in zip("QKV", (out["dq"], out["dk"], out["dv"]), g_ref):
+            assert np.isfinite(to_np(g[0, h])).all(), f"d{name} of head {h} not finite"
+            check_grad(name, to_np(g[0, h]), r, f"head {h}")
