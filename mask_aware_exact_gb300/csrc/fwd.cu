@@ -5,37 +5,45 @@
 // work, and block-wise matmul interleaved with softmax).
 //
 // The non-FULL key blocks of the query block are visited one per step. The
-// tensor cores run ahead of the softmax: S_{j+3} = Q K_{j+3}^T is issued as
+// tensor cores run ahead of the softmax: S_{j+2} = Q K_{j+2}^T is issued as
 // soon as O += P_j V_j (the last reader of its TMEM region) has completed, so
 // the S products stay off the chain softmax_j -> O += P_j V_j, and the
 // softmax warps find S_{j+1} ready when they finish step j. P_j is written
 // over S_j's own region.
+//
+// The two softmax warpgroups split every key block in halves and keep
+// separate online-softmax states: warpgroup w owns keys [64w, 64w+64) of every
+// block, its own running maximum and sum per row and its own accumulator O_w
+// = sum over its keys of P V. So the warpgroups never wait for each other
+// inside a step (no exchange of row maxima); the two states are merged once,
+// in the epilogue: with m = max(m_0, m_1) and f_w = 2^(m_w - m),
+// O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1), the exact result.
 //
 // Persistent CTAs (one per SM) take query blocks from a work counter; see the
 // kernel's comment. Warp roles (384 threads):
 //   warps 0-7  softmax, two warpgroups. Thread (w, r) owns query row r (= TMEM
 //              lane r) and key columns [64w, 64w+64) of every block: it loads
 //              its 64 S values into registers, applies the element mask on
-//              PARTIAL tiles, exchanges its partial row maximum with the other
-//              warpgroup through shared memory, keeps the running max and
-//              partial sum in fp32 (log2 domain), and writes its P slice into
-//              TMEM. O is rescaled only when the max grows by more than 2^8
-//              (lazy rescaling: exact after the final division); warpgroup w
-//              rescales O columns [w d/2, (w+1) d/2). Finally O = acc / l and LSE.
+//              PARTIAL tiles, keeps its running max and partial sum in fp32
+//              (log2 domain), and writes its P slice into TMEM. O_w is
+//              rescaled only when that max grows by more than 2^8 (lazy
+//              rescaling: exact after the final division). Epilogue: merge of
+//              the two halves, O and LSE.
 //   warp 8     work scheduler and TMA producer of Q (once per item) and K
-//              blocks (three-slot ring).
-//   warp 9     MMA issuer (one thread): per step O += P_j V_j after go(j), then
-//              S_{j+3} once that product has completed and K_{j+3} has landed.
-//   warp 10    TMA producer of V blocks (three-slot ring).
+//              blocks (two-slot ring).
+//   warp 9     MMA issuer (one thread): per step O_w += P_{j,w} V_{j,w} for both
+//              halves after go(j), then S_{j+2} once those products have
+//              completed and K_{j+2} has landed.
+//   warp 10    TMA producer of V blocks (two-slot ring).
 //   warp 11    gatekeeper (one thread): for step j waits until V_j has landed,
 //              P_j is written (and, at an item's first step, the previous O
 //              has been read out), then signals go(j), so that the MMA thread
-//              waits once per product.
+//              waits once per step.
 //
-// TMEM columns (512 allocated): S regions [0,128) [128,256) [256,384), O [384, 384+d).
-// Ordering: S_{j+3} reuses the region of S_j / P_j once O += P_j V_j has
-// completed; the softmax of step j rescales O only after O += P_{j-1} V_{j-1}
-// has completed.
+// TMEM columns (512 allocated): S regions [0,128) [128,256), O_0 [256, 256+d),
+// O_1 [384, 384+d). Ordering: S_{j+2} reuses the region of S_j / P_j once the
+// products of step j have completed; warpgroup w rescales O_w at step j only
+// after the products of step j-1 have completed.
 #include "internal.h"
 #include "ptx.cuh"
 #include "ptx_fp8.cuh"
@@ -46,9 +54,10 @@ namespace fm {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kSRegions = 3;  // TMEM S/P regions of 128 columns
-constexpr int kKSlots = 3, kVSlots = 3;
-constexpr uint32_t kColO = 384;
+constexpr int kSRegions = 2;  // TMEM S/P regions of 128 columns
+constexpr int kKSlots = 2, kVSlots = 2;
+// O accumulator of softmax warpgroup w (its half of the keys of every block)
+__device__ __forceinline__ uint32_t col_o(int w) { return 256u + 128u * static_cast<uint32_t>(w); }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // FP8: P is stored as e4m3(p * kFp8PScale). With the running maximum lagging
 // by at most kRescaleThresholdFp8 (log2 units), p < 2^threshold and
@@ -64,7 +73,7 @@ struct FwdLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;             // kKSlots x kTileBytes
   static constexpr int kV = kK + kKSlots * kTileBytes;   // kVSlots x kTileBytes
-  static constexpr int kRed = kV + kVSlots * kTileBytes;  // fp32 [2 parity][2 groups][128]
+  static constexpr int kRed = kV + kVSlots * kTileBytes;  // fp32 [m, l][2 groups][128]
   static constexpr int kBar = kRed + 2 * 2 * kTile * 4;
   // q_full, k_full[3], v_full[3], s_full[3], p_full[3], pv_done[3], go[3],
   // sched_full[2], sched_empty[2], o_free. K slot, V slot and S region of step
@@ -127,33 +136,24 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, float f) {
   }
 }
 
-// Writes n (16 or 32) TMEM columns of this lane's row, times f, as bf16 (the TMEM
-// load runs on every lane of the warp; only lanes with `store` write).
-template <int n>
-__device__ __forceinline__ void tmem_cols_to_bf16(uint32_t taddr, bool live, float f,
-                                                  uint16_t* dst, bool store) {
-  uint32_t v[n];
+// Writes n = 32 TMEM columns of this lane's row as bf16 after merging two
+// accumulators, f0 * A + f1 * B (the TMEM loads run on every lane of the warp;
+// only lanes with `store` write).
+__device__ __forceinline__ void tmem_merge_to_bf16(uint32_t ta, uint32_t tb, bool live, float f0,
+                                                   float f1, uint16_t* dst, bool store) {
+  uint32_t a[32], b[32];
   if (live) {
-    if constexpr (n == 32) {
-      tmem_ld32(taddr, v);
-    } else {
-      tmem_ld16(taddr, v);
-    }
+    tmem_ld32(ta, a);
+    tmem_ld32(tb, b);
   } else {
 #pragma unroll
-    for (int i = 0; i < n; ++i) v[i] = 0u;
+    for (int i = 0; i < 32; ++i) a[i] = b[i] = 0u;
   }
-  if (!store) return;  // after the (warp-collective) TMEM load
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  if (!store) return;  // after the (warp-collective) TMEM loads
 #pragma unroll
-  for (int i = 0; i < n / 8; ++i) {
-    uint4 q4;
-    q4.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]) * f, __uint_as_float(v[8 * i + 1]) * f);
-    q4.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * f, __uint_as_float(v[8 * i + 3]) * f);
-    q4.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * f, __uint_as_float(v[8 * i + 5]) * f);
-    q4.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * f, __uint_as_float(v[8 * i + 7]) * f);
-    d4[i] = q4;
-  }
+  for (int i = 0; i < 32; ++i)
+    a[i] = __float_as_uint(__uint_as_float(a[i]) * f0 + __uint_as_float(b[i]) * f1);
+  store_row32_bf16(dst, a, 1.f);
 }
 
 // kShortLast: N is not a multiple of 128. kFp8 (d = 128 only): e4m3 Q, K and
@@ -412,15 +412,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kPvSteps; ++kk) {
-            // A: P, 8 TMEM columns per K step; B: the next 16 key rows of V
-            // (bf16) or the next 32 key bytes of each row of V^T (e4m3)
-            if constexpr (kFp8)
-              mma_ts_f8(tmem + kColO, tmem + 128 * g + 8 * kk,
-                        vd + static_cast<uint64_t>((kk * 32) >> 4), idesc_pv, (j > 0 || kk > 0));
-            else
-              mma_ts(tmem + kColO, tmem + 128 * g + 8 * kk,
-                     vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (j > 0 || kk > 0));
+          for (int w = 0; w < 2; ++w) {
+#pragma unroll
+            for (int kk = 0; kk < kPvSteps / 2; ++kk) {
+              // O_w += P_w V_w over keys [64w, 64w+64): A = P_w, 8 TMEM
+              // columns per K step from column 64w (bf16 pairs or e4m3
+              // quads); B = the next 16 key rows of V (bf16) or the next 32
+              // key bytes of each row of V^T (e4m3)
+              if constexpr (kFp8)
+                mma_ts_f8(tmem + col_o(w), tmem + 128 * g + 64 * w + 8 * kk,
+                          vd + static_cast<uint64_t>((64 * w + kk * 32) >> 4), idesc_pv,
+                          (j > 0 || kk > 0));
+              else
+                mma_ts(tmem + col_o(w), tmem + 128 * g + 64 * w + 8 * kk,
+                       vd + static_cast<uint64_t>(((4 * w + kk) * 2048) >> 4), idesc_pv,
+                       (j > 0 || kk > 0));
+            }
           }
           mma_commit(bar.pv_done(g));  // also frees V slot J % 3
           if (j + kSRegions < ntiles) ok = issue_s(Jj + kSRegions);
@@ -541,14 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
         }
-        // exchange the two partial row maxima (double-buffered by step parity);
-        // the barrier also orders both warpgroups' S loads before any P store
-        // into the region
-        red[((Jj & 1) * 2 + w) * kTile + row] = pm;
-        softmax_bar();
         if (ok) {
-          const float mx = fmaxf(pm, red[((Jj & 1) * 2 + (w ^ 1)) * kTile + row]);
-          const float m_new = fmaxf(m, mx);
+          // this warpgroup's own running maximum over its half of the keys
+          const float m_new = fmaxf(m, pm);
           const bool rescale = m_new > m + kThresh;
           float alpha = 1.f;
           if (rescale) {
@@ -583,24 +585,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           float l0, l1;
           f2_split(l2, l0, l1);
           l = l * alpha + (l0 + l1);
-          // P_j over this warpgroup's part of S_j's region: keys [64w, 64w+64)
-          // as bf16 pairs in columns [32w, 32w+32) (the A operand of P V)
+          // P_j over the S columns this warpgroup has just read (the other
+          // warpgroup may still be reading its own): keys [64w, 64w+64) as
+          // bf16 pairs in columns [64w, 64w+32) (the A operand of P V)
           if constexpr (kFp8) {
-            // ... or as e4m3 quads in columns [16w, 16w+16)
-            tmem_st16(tmem + lane_base + 128 * g + 16 * w,
+            // ... or as e4m3 quads in columns [64w, 64w+16)
+            tmem_st16(tmem + lane_base + 128 * g + 64 * w,
                       *reinterpret_cast<const uint32_t(*)[16]>(pk));
           } else {
-            tmem_st32p(tmem + lane_base + 128 * g + 32 * w, pk);
+            tmem_st32p(tmem + lane_base + 128 * g + 64 * w, pk);
           }
           if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-            // O is rescaled once O += P_{j-1} V_{j-1} has completed
+            // O_w is rescaled once the products of step j-1 have completed
             ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done((Jj - 1) % kSRegions),
                                                    ((Jj - 1) / kSRegions) & 1, p.status));
             if (ok) {
               tc_fence_after();
 #pragma unroll
-              for (int ch = 0; ch < kOCols / 32; ++ch)
-                tmem_scale_cols<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, alpha);
+              for (int ch = 0; ch < D / 32; ++ch)
+                tmem_scale_cols<32>(tmem + lane_base + col_o(w) + 32 * ch, alpha);
             } else if (lane == 0) {
               record_failure(p.status, kStatusTimeout, kSiteFwdO);
             }
@@ -619,38 +622,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdO);
         tc_fence_after();
       }
-      // row sums through the exchange buffer of the parity the item's last
-      // step did not use (its readers passed that step's barrier)
-      float* lsum = red + ((J + ntiles) & 1) * 2 * kTile;
-      lsum[w * kTile + row] = l;
+      // merge the two halves' states: each warpgroup publishes its row maximum
+      // and sum, then writes its half of the output columns from both
+      // accumulators, O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1)
+      red[w * kTile + row] = m;
+      red[(2 + w) * kTile + row] = l;
       softmax_bar();
-      const float ltot = l + lsum[(w ^ 1) * kTile + row];
+      const float m_o = red[(w ^ 1) * kTile + row], l_o = red[(2 + (w ^ 1)) * kTile + row];
+      const float m_all = fmaxf(m, m_o);
+      const float f_self = (m == -INFINITY) ? 0.f : ex2(m - m_all);
+      const float f_oth = (m_o == -INFINITY) ? 0.f : ex2(m_o - m_all);
+      const float ltot = l * f_self + l_o * f_oth;
       const bool live = ok && ntiles > 0;
       const bool has = live && ltot > 0.f;
       // FP8: O accumulated (kFp8PScale P) (V / scale_V)
       const float inv = has ? (kFp8 ? p.vscale[bh] * (1.f / kFp8PScale) : 1.f) / ltot : 0.f;
+      const float f0 = (w == 0 ? f_self : f_oth) * inv, f1 = (w == 0 ? f_oth : f_self) * inv;
       // rows >= N of a short last query block do not exist: nothing is stored
       const bool row_exists = !kShortLast || r * kTile + row < p.N;
       uint16_t* orow = p.o + static_cast<size_t>(it.q_row0 + row) * D + w * kOCols;
 #pragma unroll
       for (int ch = 0; ch < kOCols / 32; ++ch)
-        tmem_cols_to_bf16<32>(tmem + lane_base + kColO + w * kOCols + 32 * ch, live, inv,
-                              orow + 32 * ch, row_exists);
+        tmem_merge_to_bf16(tmem + lane_base + col_o(0) + w * kOCols + 32 * ch,
+                           tmem + lane_base + col_o(1) + w * kOCols + 32 * ch, live, f0, f1,
+                           orow + 32 * ch, row_exists);
       if (ntiles > 0) {
-        // O has been read (the loads above completed): the next item's first
-        // O += P V may overwrite it
+        // O_0 and O_1 have been read (the loads above completed): the next
+        // item's first products may overwrite them
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar.o_free());
       }
       if (w == 0 && row_exists) {
-        const float m_fin = (m == -INFINITY) ? 0.f : m;
+        const float m_fin = (m_all == -INFINITY) ? 0.f : m_all;
         p.lse[it.q_row0 + row] =
             has ? (m_fin + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
       }
       J += ntiles;
-      // every warp has read lsum before the next item's first step (or
-      // epilogue) writes the same buffer
+      // every warp has read the exchange buffer before the next item's
+      // epilogue writes it
       softmax_bar();
     }
   }
