@@ -58,8 +58,8 @@ E2E_CHUNK_HEADS = 2
 # scaled by 4 to H = 32: every head is an independent unit of identical work,
 # so traffic grows in proportion to the heads.
 NCU_TRAFFIC = {
-    "bwd_main@172b1ff61d70@document_b1h32n32768d128": 4 * (405.954048e6 + 220.839424e6),
-    "fwd@176d56817e16@document_b1h32n32768d128": 4 * (201.946624e6 + 49.924608e6),
+    "bwd_main@6f64dc63d5fd@document_b1h32n32768d128": 4 * (405.986048e6 + 220.411392e6),
+    "fwd@c52e9fb7944e@document_b1h32n32768d128": 4 * (202.131712e6 + 49.547008e6),
 }
 
 
