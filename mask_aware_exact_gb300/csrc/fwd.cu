@@ -31,14 +31,19 @@
 //              the two halves, O and LSE.
 //   warp 8     work scheduler and TMA producer of Q (once per item) and K
 //              blocks (two-slot ring).
-//   warp 9     MMA issuer (one thread): per step O_w += P_{j,w} V_{j,w} for both
-//              halves after go(j), then S_{j+2} once those products have
-//              completed and K_{j+2} has landed.
+//   warp 9     S issuer (one thread): S_j once K_j has landed and the P V
+//              products of step j-2 (the last readers of its TMEM region)
+//              have completed.
 //   warp 10    TMA producer of V blocks (two-slot ring).
-//   warp 11    gatekeeper (one thread): for step j waits until V_j has landed,
-//              P_j is written (and, at an item's first step, the previous O
-//              has been read out), then signals go(j), so that the MMA thread
-//              waits once per step.
+//   warp 11    P V issuer (one thread): for step j waits until V_j has landed
+//              and both halves of P_j are written (and, at an item's first
+//              step, the previous item's O_0 and O_1 have been read out), then
+//              issues O_w += P_{j,w} V_{j,w} for both halves.
+//   S and P V come from two threads so that neither waits behind the other:
+//   one thread issuing both spends each step issuing P V, waiting for those
+//   products to complete (the next S overwrites the columns they read) and
+//   issuing S, about 2000 cycles per step in a clock64 trace, during which
+//   the softmax warps waited for S.
 //
 // TMEM columns (512 allocated): S regions [0,128) [128,256), O_0 [256, 256+d),
 // O_1 [384, 384+d). Ordering: S_{j+2} reuses the region of S_j / P_j once the
@@ -75,12 +80,12 @@ struct FwdLayout {
   static constexpr int kV = kK + kKSlots * kTileBytes;   // kVSlots x kTileBytes
   static constexpr int kRed = kV + kVSlots * kTileBytes;  // fp32 [m, l][2 groups][128]
   static constexpr int kBar = kRed + 2 * 2 * kTile * 4;
-  // q_full, k_full[3], v_full[3], s_full[3], p_full[3], pv_done[3], go[3],
+  // q_full, k_full[2], v_full[2], s_full[2], p_full[2], pv_done[2],
   // sched_full[2], sched_empty[2], o_free. K slot, V slot and S region of step
-  // J are all J % 3, so "S_J done" also frees K slot J % 3 and "P_J V_J done"
-  // also frees V slot J % 3.
+  // J are all J % 2, so "S_J done" also frees K slot J % 2 and "P_J V_J done"
+  // also frees V slot J % 2.
   static_assert(kKSlots == kSRegions && kVSlots == kSRegions, "slots follow the S regions");
-  static constexpr int kNumBars = 1 + kKSlots + kVSlots + 4 * kSRegions + 5;
+  static constexpr int kNumBars = 1 + kKSlots + kVSlots + 3 * kSRegions + 5;
   static constexpr int kSched = kBar + kNumBars * 8;  // int[4]
   static constexpr int kTmemSlot = kSched + 16;
   static constexpr int kBytes = kTmemSlot + 16;
@@ -98,20 +103,17 @@ struct FwdBars {
   __device__ uint32_t pv_done(int r) const {
     return base + 8 * (1 + kKSlots + kVSlots + 2 * kSRegions + r);
   }
-  __device__ uint32_t go(int r) const {
-    return base + 8 * (1 + kKSlots + kVSlots + 3 * kSRegions + r);
-  }
   __device__ uint32_t sched_full(int s) const {
-    return base + 8 * (1 + kKSlots + kVSlots + 4 * kSRegions + s);
+    return base + 8 * (1 + kKSlots + kVSlots + 3 * kSRegions + s);
   }
   __device__ uint32_t sched_empty(int s) const {
-    return base + 8 * (3 + kKSlots + kVSlots + 4 * kSRegions + s);
+    return base + 8 * (3 + kKSlots + kVSlots + 3 * kSRegions + s);
   }
-  __device__ uint32_t o_free() const { return base + 8 * (5 + kKSlots + kVSlots + 4 * kSRegions); }
+  __device__ uint32_t o_free() const { return base + 8 * (5 + kKSlots + kVSlots + 3 * kSRegions); }
 };
 
-// Roles that read each published work item: the MMA issuer, the V producer,
-// the gatekeeper and softmax warp 0 (which shares it with the other seven).
+// Roles that read each published work item: the S issuer, the P V issuer, the
+// V producer and softmax warp 0 (which shares it with the other seven).
 constexpr int kSchedReaders = 4;
 
 
@@ -206,7 +208,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar.s_full(g), 1);
       mbar_init(bar.p_full(g), 8);
       mbar_init(bar.pv_done(g), 1);
-      mbar_init(bar.go(g), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar.sched_full(s), 1);
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = atomicAdd(p.sched, 1);
         return n < n_items ? n : -1;
       };
-      // K of step J into slot J % 3 once S_{J-3} has completed; kb is the
+      // K of step J into slot J % 2 once S_{J-2} has completed; kb is the
       // key block, bh the head (3-D map: rows past the head's end read zeros)
       auto load_k = [&](int J, int kb, int bh) -> bool {
         const int slot = J % kKSlots;
@@ -345,47 +346,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = kFp8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, 0, 1);
       constexpr int kSSteps = kFp8 ? D / 32 : D / 16;  // K steps of S = Q K^T
-      constexpr int kPvSteps = kFp8 ? 4 : 8;           // K steps (keys) of O += P V
       // Shared-memory descriptors are built once: the address field (bits
       // 0-13, in 16-byte units) of every operand stays below 2^14 here, so a
       // descriptor for base + off is the base descriptor plus off / 16. This
       // keeps the per-MMA instruction stream of this thread short.
       const uint64_t dq_base = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk_base = sdesc_sw128(sK, 16, 1024);
-      // V is MN-major [keys][d] in bf16, K-major [d][keys] as e4m3 V^T
-      const uint64_t dv_base = kFp8 ? sdesc_sw128(sV, 16, 1024) : sdesc_sw128(sV, 16384, 1024);
-      // S of step J into region J % 3 once K_J has landed and O += P V of
-      // step J - 3 (the last reader of that region) has completed
-      auto issue_s = [&](int J) -> bool {
-        const int slot = J % kKSlots, g = J % kSRegions;
-        if (J >= kSRegions &&
-            !mbar_wait(bar.pv_done(g), ((J / kSRegions) - 1) & 1, p.status)) {
-          record_failure(p.status, kStatusTimeout, kSiteFwdO);
-          return false;
-        }
-        if (!mbar_wait(bar.k_full(slot), (J / kKSlots) & 1, p.status)) {
-          record_failure(p.status, kStatusTimeout, kSiteFwdK);
-          return false;
-        }
-        tc_fence_after();
-        const uint64_t kd = dk_base + static_cast<uint64_t>((slot * L::kTileBytes) >> 4);
-#pragma unroll
-        for (int k = 0; k < kSSteps; ++k) {
-          // 32 bytes of each 128-byte row per K step (16 bf16 or 32 e4m3)
-          const uint64_t off16 = static_cast<uint64_t>(((k >> 2) * L::kChunk + (k & 3) * 32) >> 4);
-          if constexpr (kFp8)
-            mma_ss_f8(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, k > 0);
-          else
-            mma_ss(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, k > 0);
-        }
-        mma_commit(bar.s_full(g));  // also frees K slot J % 3
-        return true;
-      };
       bool ok = true;
       int J = 0, ti = 0;  // running step; items with tiles so far
       for (int k = 0; ok; ++k) {
@@ -397,16 +367,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           record_failure(p.status, kStatusTimeout, kSiteFwdQ);
           break;
         }
-        tc_fence_after();
-        // S runs three steps ahead of O += P V: the item's first three now,
-        // then S_{J+3} right after O += P_J V_J (same region) has completed,
-        // which keeps S off the softmax -> P V chain
-        for (int m = 0; ok && m < kSRegions && m < ntiles; ++m) ok = issue_s(J + m);
-        for (int j = 0; ok && j < ntiles; ++j) {
-          const int Jj = J + j, g = Jj % kSRegions, vs = Jj % kVSlots;
-          if (!mbar_wait(bar.go(g), (Jj / kSRegions) & 1, p.status)) {
-            record_failure(p.status, kStatusTimeout, kSiteFwdP);
+        // S of step J into region J % 2 once K_J has landed and the P V
+        // products of step J - 2 (the last readers of that region) have
+        // completed; this thread waits only for those, never for the
+        // softmax, so S runs up to two steps ahead of the P V products
+        for (int j = 0; ok && j < ntiles; ++j, ++J) {
+          const int slot = J % kKSlots, g = J % kSRegions;
+          if (J >= kSRegions &&
+              !mbar_wait(bar.pv_done(g), ((J / kSRegions) - 1) & 1, p.status)) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdO);
             ok = false;
+            break;
+          }
+          if (!mbar_wait(bar.k_full(slot), (J / kKSlots) & 1, p.status)) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdK);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kd = dk_base + static_cast<uint64_t>((slot * L::kTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kSSteps; ++kk) {
+            // 32 bytes of each 128-byte row per K step (16 bf16 or 32 e4m3)
+            const uint64_t off16 =
+                static_cast<uint64_t>(((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4);
+            if constexpr (kFp8)
+              mma_ss_f8(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, kk > 0);
+            else
+              mma_ss(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, kk > 0);
+          }
+          mma_commit(bar.s_full(g));  // also frees K slot J % 2
+        }
+        ++ti;
+      }
+    }
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ P V issuer
+    // For step j: waits until V_j has landed, both halves of P_j are written
+    // (and, at an item's first step, the previous item's O_0 and O_1 have been
+    // read out), then issues O_w += P_{j,w} V_{j,w} for both halves.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = kFp8 ? idesc_e4m3(128, D) : idesc_bf16(128, D, 0, 1);
+      constexpr int kPvSteps = kFp8 ? 4 : 8;  // K steps (keys) of O += P V
+      // V is MN-major [keys][d] in bf16, K-major [d][keys] as e4m3 V^T
+      const uint64_t dv_base = kFp8 ? sdesc_sw128(sV, 16, 1024) : sdesc_sw128(sV, 16384, 1024);
+      bool ok = true;
+      int J = 0, ti = 0;
+      for (int k = 0; ok; ++k) {
+        const int n = read_item(k, ok);
+        if (n < 0) break;
+        const int ntiles = decode(n).ntiles;
+        if (ntiles == 0) continue;
+        for (int j = 0; j < ntiles; ++j, ++J) {
+          const int g = J % kSRegions, vs = J % kVSlots;
+          ok = mbar_wait(bar.v_full(vs), (J / kVSlots) & 1, p.status);
+          // the item's first products overwrite O_0 and O_1: the previous
+          // item's accumulators must have been read out
+          if (j == 0 && ti > 0) ok = ok && mbar_wait(bar.o_free(), (ti - 1) & 1, p.status);
+          ok = ok && mbar_wait(bar.p_full(g), (J / kSRegions) & 1, p.status);
+          if (!ok) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdP);
             break;
           }
           tc_fence_after();
@@ -429,35 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (j > 0 || kk > 0));
             }
           }
-          mma_commit(bar.pv_done(g));  // also frees V slot J % 3
-          if (j + kSRegions < ntiles) ok = issue_s(Jj + kSRegions);
-        }
-        J += ntiles;
-        ++ti;
-      }
-    }
-  } else if (warp == 11) {
-    // ------------------------------------------------------------ gatekeeper
-    if (lane == 0) {
-      bool ok = true;
-      int J = 0, ti = 0;
-      for (int k = 0; ok; ++k) {
-        const int n = read_item(k, ok);
-        if (n < 0) break;
-        const int ntiles = decode(n).ntiles;
-        if (ntiles == 0) continue;
-        for (int j = 0; j < ntiles; ++j, ++J) {
-          const int g = J % kSRegions;
-          ok = mbar_wait(bar.v_full(J % kVSlots), (J / kVSlots) & 1, p.status);
-          // the item's first O += P V overwrites O: the previous item's O must
-          // have been read out
-          if (j == 0 && ti > 0) ok = ok && mbar_wait(bar.o_free(), (ti - 1) & 1, p.status);
-          ok = ok && mbar_wait(bar.p_full(g), (J / kSRegions) & 1, p.status);
-          if (!ok) {
-            record_failure(p.status, kStatusTimeout, kSiteFwdP);
-            break;
-          }
-          mbar_arrive(bar.go(g));
+          mma_commit(bar.pv_done(g));  // also frees V slot J % 2
         }
         ++ti;
       }
