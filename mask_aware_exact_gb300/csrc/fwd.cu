@@ -80,14 +80,12 @@ struct FwdLayout {
   static constexpr int kV = kK + kKSlots * kTileBytes;   // kVSlots x kTileBytes
   static constexpr int kRed = kV + kVSlots * kTileBytes;  // fp32 [m, l][2 groups][128]
   static constexpr int kBar = kRed + 2 * 2 * kTile * 4;
-  // q_full, k_full[2], v_full[2], then per (S region g, key half w):
-  // s_full[2][2], p_full[2][2], pv_done[2][2]; sched_full[2], sched_empty[2],
-  // o_free. K slot, V slot and S region of step J are all J % 2; each half's
-  // S and P V are committed after the other half's (half 1 after half 0), so
-  // "S_{J,1} done" also frees K slot J % 2 and "P_{J,1} V done" also frees V
-  // slot J % 2.
+  // q_full, k_full[2], v_full[2], s_full[2], p_full[2], pv_done[2],
+  // sched_full[2], sched_empty[2], o_free. K slot, V slot and S region of step
+  // J are all J % 2, so "S_J done" also frees K slot J % 2 and "P_J V_J done"
+  // also frees V slot J % 2.
   static_assert(kKSlots == kSRegions && kVSlots == kSRegions, "slots follow the S regions");
-  static constexpr int kNumBars = 1 + kKSlots + kVSlots + 6 * kSRegions + 5;
+  static constexpr int kNumBars = 1 + kKSlots + kVSlots + 3 * kSRegions + 5;
   static constexpr int kSched = kBar + kNumBars * 8;  // int[4]
   static constexpr int kTmemSlot = kSched + 16;
   static constexpr int kBytes = kTmemSlot + 16;
@@ -95,20 +93,23 @@ struct FwdLayout {
 
 struct FwdBars {
   uint32_t base;
-  static constexpr int kH = 1 + kKSlots + kVSlots;  // first per-(region, half) barrier
   __device__ uint32_t q_full() const { return base; }
   __device__ uint32_t k_full(int s) const { return base + 8 * (1 + s); }
   __device__ uint32_t v_full(int s) const { return base + 8 * (1 + kKSlots + s); }
-  __device__ uint32_t s_full(int r, int w) const { return base + 8 * (kH + 2 * r + w); }
-  __device__ uint32_t p_full(int r, int w) const {
-    return base + 8 * (kH + 2 * kSRegions + 2 * r + w);
+  __device__ uint32_t s_full(int r) const { return base + 8 * (1 + kKSlots + kVSlots + r); }
+  __device__ uint32_t p_full(int r) const {
+    return base + 8 * (1 + kKSlots + kVSlots + kSRegions + r);
   }
-  __device__ uint32_t pv_done(int r, int w) const {
-    return base + 8 * (kH + 4 * kSRegions + 2 * r + w);
+  __device__ uint32_t pv_done(int r) const {
+    return base + 8 * (1 + kKSlots + kVSlots + 2 * kSRegions + r);
   }
-  __device__ uint32_t sched_full(int s) const { return base + 8 * (kH + 6 * kSRegions + s); }
-  __device__ uint32_t sched_empty(int s) const { return base + 8 * (kH + 6 * kSRegions + 2 + s); }
-  __device__ uint32_t o_free() const { return base + 8 * (kH + 6 * kSRegions + 4); }
+  __device__ uint32_t sched_full(int s) const {
+    return base + 8 * (1 + kKSlots + kVSlots + 3 * kSRegions + s);
+  }
+  __device__ uint32_t sched_empty(int s) const {
+    return base + 8 * (3 + kKSlots + kVSlots + 3 * kSRegions + s);
+  }
+  __device__ uint32_t o_free() const { return base + 8 * (5 + kKSlots + kVSlots + 3 * kSRegions); }
 };
 
 // Roles that read each published work item: the S issuer, the P V issuer, the
@@ -204,11 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kKSlots; ++s) mbar_init(bar.k_full(s), 1);
     for (int s = 0; s < kVSlots; ++s) mbar_init(bar.v_full(s), 1);
     for (int g = 0; g < kSRegions; ++g) {
-      for (int w = 0; w < 2; ++w) {
-        mbar_init(bar.s_full(g, w), 1);
-        mbar_init(bar.p_full(g, w), 4);
-        mbar_init(bar.pv_done(g, w), 1);
-      }
+      mbar_init(bar.s_full(g), 1);
+      mbar_init(bar.p_full(g), 8);
+      mbar_init(bar.pv_done(g), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar.sched_full(s), 1);
@@ -269,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_k = [&](int J, int kb, int bh) -> bool {
         const int slot = J % kKSlots;
         if (J >= kKSlots &&
-            !mbar_wait(bar.s_full(slot, 1), ((J / kKSlots) - 1) & 1, p.status)) {
+            !mbar_wait(bar.s_full(slot), ((J / kKSlots) - 1) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteFwdKEmpty);
           return false;
         }
@@ -288,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = decode(cur);
         if (it.ntiles > 0) {
           // the Q buffer is free once the last S of the previous item is done
-          if (J_last >= 0 && !mbar_wait(bar.s_full(J_last % kSRegions, 1),
+          if (J_last >= 0 && !mbar_wait(bar.s_full(J_last % kSRegions),
                                         (J_last / kSRegions) & 1, p.status)) {
             record_failure(p.status, kStatusTimeout, kSiteFwdKEmpty);
             ok = false;
@@ -328,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < it.ntiles; ++j, ++J) {
           const int slot = J % kVSlots;
           if (J >= kVSlots &&
-              !mbar_wait(bar.pv_done(slot, 1), ((J / kVSlots) - 1) & 1, p.status)) {
+              !mbar_wait(bar.pv_done(slot), ((J / kVSlots) - 1) & 1, p.status)) {
             record_failure(p.status, kStatusTimeout, kSiteFwdVEmpty);
             ok = false;
             break;
@@ -349,8 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ S issuer
     if (lane == 0) {
-      // S halves: M = 128 queries, N = 64 keys
-      constexpr uint32_t idesc_s = kFp8 ? idesc_e4m3(128, 64) : idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t idesc_s = kFp8 ? idesc_e4m3(128, 128) : idesc_bf16(128, 128, 0, 0);
       constexpr int kSSteps = kFp8 ? D / 32 : D / 16;  // K steps of S = Q K^T
       // Shared-memory descriptors are built once: the address field (bits
       // 0-13, in 16-byte units) of every operand stays below 2^14 here, so a
@@ -369,45 +367,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           record_failure(p.status, kStatusTimeout, kSiteFwdQ);
           break;
         }
-        // S of step J into region J % 2, one half of the keys at a time: half
-        // w (keys [64w, 64w+64), TMEM columns [64w, 64w+64) of the region,
-        // read only by softmax warpgroup w) once K_J has landed and the P V
-        // product of half w of step J - 2 (the last reader of those columns)
-        // has completed. This thread never waits for the softmax, and one
-        // half never waits for the other's products.
+        // S of step J into region J % 2 once K_J has landed and the P V
+        // products of step J - 2 (the last readers of that region) have
+        // completed; this thread waits only for those, never for the
+        // softmax, so S runs up to two steps ahead of the P V products
         for (int j = 0; ok && j < ntiles; ++j, ++J) {
           const int slot = J % kKSlots, g = J % kSRegions;
+          if (J >= kSRegions &&
+              !mbar_wait(bar.pv_done(g), ((J / kSRegions) - 1) & 1, p.status)) {
+            record_failure(p.status, kStatusTimeout, kSiteFwdO);
+            ok = false;
+            break;
+          }
           if (!mbar_wait(bar.k_full(slot), (J / kKSlots) & 1, p.status)) {
             record_failure(p.status, kStatusTimeout, kSiteFwdK);
             ok = false;
             break;
           }
+          tc_fence_after();
           const uint64_t kd = dk_base + static_cast<uint64_t>((slot * L::kTileBytes) >> 4);
 #pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            if (J >= kSRegions &&
-                !mbar_wait(bar.pv_done(g, w), ((J / kSRegions) - 1) & 1, p.status)) {
-              record_failure(p.status, kStatusTimeout, kSiteFwdO);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kSSteps; ++kk) {
-              // 32 bytes of each 128-byte row per K step (16 bf16 or 32 e4m3);
-              // the half's 64 key rows start 64 rows (8 KB) into each chunk
-              const uint64_t off16 =
-                  static_cast<uint64_t>(((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4);
-              const uint64_t half16 = static_cast<uint64_t>((w * 8192) >> 4);
-              if constexpr (kFp8)
-                mma_ss_f8(tmem + 128 * g + 64 * w, dq_base + off16, kd + off16 + half16, idesc_s,
-                          kk > 0);
-              else
-                mma_ss(tmem + 128 * g + 64 * w, dq_base + off16, kd + off16 + half16, idesc_s,
-                       kk > 0);
-            }
-            mma_commit(bar.s_full(g, w));  // half 1: also frees K slot J % 2
+          for (int kk = 0; kk < kSSteps; ++kk) {
+            // 32 bytes of each 128-byte row per K step (16 bf16 or 32 e4m3)
+            const uint64_t off16 =
+                static_cast<uint64_t>(((kk >> 2) * L::kChunk + (kk & 3) * 32) >> 4);
+            if constexpr (kFp8)
+              mma_ss_f8(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, kk > 0);
+            else
+              mma_ss(tmem + 128 * g, dq_base + off16, kd + off16, idesc_s, kk > 0);
           }
+          mma_commit(bar.s_full(g));  // also frees K slot J % 2
         }
         ++ti;
       }
@@ -435,20 +424,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the item's first products overwrite O_0 and O_1: the previous
           // item's accumulators must have been read out
           if (j == 0 && ti > 0) ok = ok && mbar_wait(bar.o_free(), (ti - 1) & 1, p.status);
+          ok = ok && mbar_wait(bar.p_full(g), (J / kSRegions) & 1, p.status);
           if (!ok) {
             record_failure(p.status, kStatusTimeout, kSiteFwdP);
             break;
           }
+          tc_fence_after();
           const uint64_t vd = dv_base + static_cast<uint64_t>((vs * L::kTileBytes) >> 4);
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
-            // half w as soon as softmax warpgroup w has written its P
-            if (!mbar_wait(bar.p_full(g, w), (J / kSRegions) & 1, p.status)) {
-              record_failure(p.status, kStatusTimeout, kSiteFwdP);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kPvSteps / 2; ++kk) {
               // O_w += P_w V_w over keys [64w, 64w+64): A = P_w, 8 TMEM
@@ -464,9 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        vd + static_cast<uint64_t>(((4 * w + kk) * 2048) >> 4), idesc_pv,
                        (j > 0 || kk > 0));
             }
-            mma_commit(bar.pv_done(g, w));  // half 1: also frees V slot J % 2
           }
-          if (!ok) break;
+          mma_commit(bar.pv_done(g));  // also frees V slot J % 2
         }
         ++ti;
       }
@@ -533,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
           ok = __all_sync(0xffffffffu,
-                          mbar_wait(bar.s_full(g, w), (Jj / kSRegions) & 1, p.status));
+                          mbar_wait(bar.s_full(g), (Jj / kSRegions) & 1, p.status));
           if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdS);
         }
         uint32_t sv[64];
@@ -606,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
             // O_w is rescaled once the products of step j-1 have completed
-            ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done((Jj - 1) % kSRegions, w),
+            ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done((Jj - 1) % kSRegions),
                                                    ((Jj - 1) / kSRegions) & 1, p.status));
             if (ok) {
               tc_fence_after();
@@ -621,14 +604,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar.p_full(g, w));
+        if (lane == 0) mbar_arrive(bar.p_full(g));
       }
       // ---------------------------------------------------------- epilogue of the item
       if (ok && ntiles > 0) {
         const int jl = J + ntiles - 1;
-        // the merge reads both accumulators; half 1's products were issued
-        // after half 0's, so their completion covers both
-        ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(jl % kSRegions, 1),
+        ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(jl % kSRegions),
                                                (jl / kSRegions) & 1, p.status));
         if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdO);
         tc_fence_after();
