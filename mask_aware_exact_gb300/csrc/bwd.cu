@@ -22,14 +22,10 @@
 //               TMA engine.)
 //   dq_convert  dQ = bf16(scale * accumulator).
 //
-// Warp roles of bwd_kernel (480 threads): warps 0-7 compute, two warpgroups;
+// Warp roles of bwd_kernel (448 threads): warps 0-7 compute, two warpgroups;
 // warpgroup g handles queries [64g, 64g+64) of every tile and thread (g, t)
 // owns key t (= TMEM lane t). Warps 8-11 drain dQ_t (thread t = query t),
-// warp 12 is the TMA producer, warp 13 issues S^T and dP^T, warp 14 issues
-// dV, dK and dQ. With one issuing thread for all five products, S^T of the
-// next tile waited behind dK and dQ of the current one, which wait for the
-// compute warps' dS, so the compute warps finished dS and then waited for
-// S^T.
+// warp 12 is the TMA producer, warp 13 the MMA issuer.
 //
 // TMEM columns (512): S^T / P^T [0,128)  dP^T / dQ_t [128,256)
 //                     dV [256, 256+d)    dK [384, 384+d)
@@ -44,7 +40,7 @@ namespace fm {
 namespace {
 
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
-constexpr int kThreads = 480;
+constexpr int kThreads = 448;
 
 // TMEM column of the P^T operand for queries [16k, 16k+16) (A of the dV MMA).
 __device__ __forceinline__ uint32_t pt_col(int k) { return kColS + 8 * k + (k >= 4 ? 32 : 0); }
@@ -268,18 +264,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 13) {
-    // ------------------------------------------------------------ S^T, dP^T issuer
-    // The products that read Q and dO against K and V. S^T of tile t waits
-    // only for dV of tile t-1 (the last reader of P^T in the same columns),
-    // dP^T for the drain of dQ of tile t-1 (same columns): neither waits for
-    // the compute warps' dS, so the next tile's S^T is ready when they need it.
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t id_st = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
+      constexpr uint32_t id_kd = idesc_bf16(128, D, 0, 1);    // dV, dK
+      constexpr uint32_t id_dq = idesc_bf16(128, D, 1, 1);    // dQ (M = queries)
       // Shared-memory descriptors are built once: every operand address here
       // keeps the descriptor's 14-bit address field (16-byte units) below
       // 2^14, so the descriptor of base + off is the base's plus off / 16.
       const uint64_t kK = sdesc_sw128(sK, 16, 1024), kV = sdesc_sw128(sV, 16, 1024);
       const uint64_t kQ = sdesc_sw128(sQ, 16, 1024), kDO = sdesc_sw128(sDO, 16, 1024);
+      const uint64_t kDS = sdesc_sw128(sDS, 16, 1024);
+      const uint64_t mDO = sdesc_sw128(sDO, 16384, 1024), mQ = sdesc_sw128(sQ, 16384, 1024);
+      const uint64_t mDS = sdesc_sw128(sDS, 16384, 1024), mK = sdesc_sw128(sK, 16384, 1024);
       auto d16 = [](uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); };
       bool ok = mbar_wait(bar.kv_full(), 0, p.status);
       if (!ok) record_failure(p.status, kStatusTimeout, kSiteBwdKV);
@@ -316,26 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + kColDP, kV + off, kDO + stage + off, id_st, k > 0);
         }
         mma_commit(bar.dp_full());
-      }
-    }
-  } else if (warp == 14) {
-    // ------------------------------------------------------------ dV, dK, dQ issuer
-    // The products that consume the compute warps' P^T (dV) and dS (dK, dQ).
-    if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t id_kd = idesc_bf16(128, D, 0, 1);    // dV, dK
-      constexpr uint32_t id_dq = idesc_bf16(128, D, 1, 1);    // dQ (M = queries)
-      const uint64_t kDS = sdesc_sw128(sDS, 16, 1024);
-      const uint64_t mDO = sdesc_sw128(sDO, 16384, 1024), mQ = sdesc_sw128(sQ, 16384, 1024);
-      const uint64_t mDS = sdesc_sw128(sDS, 16384, 1024), mK = sdesc_sw128(sK, 16384, 1024);
-      auto d16 = [](uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); };
-      bool ok = mbar_wait(bar.kv_full(), 0, p.status);
-      if (!ok) record_failure(p.status, kStatusTimeout, kSiteBwdKV);
-      for (int t = 0; ok && t < ntiles; ++t) {
-        const int st = t & 1;
-        const uint64_t stage = d16(st * L::kTileBytes);
-        // P^T_t written (the compute warps saw Q_t land); dO_t landed
-        if (!mbar_wait(bar.pt_ready(), t & 1, p.status) ||
-            !mbar_wait(bar.do_full(st), (t >> 1) & 1, p.status)) {
+        if (!mbar_wait(bar.pt_ready(), t & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteBwdPT);
           break;
         }
