@@ -59,7 +59,7 @@ E2E_CHUNK_HEADS = 2
 # so traffic grows in proportion to the heads.
 NCU_TRAFFIC = {
     "bwd_main@6f64dc63d5fd@document_b1h32n32768d128": 4 * (405.986048e6 + 220.411392e6),
-    "fwd@c52e9fb7944e@document_b1h32n32768d128": 4 * (202.131712e6 + 49.547008e6),
+    "fwd@f75aca89249c@document_b1h32n32768d128": 4 * (202.041088e6 + 49.646848e6),
 }
 
 
