@@ -530,15 +530,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = 0; jj < 64; ++jj)
               sv[jj] = ((mbits[jj >> 5] >> (jj & 31)) & 1u) ? 0xff800000u : sv[jj];
           }
+          // four independent chains of three-input maxima over the 64 columns
           float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-          for (int jj = 0; jj < 64; jj += 4) {
-            mx0 = fmaxf(mx0, __uint_as_float(sv[jj]));
-            mx1 = fmaxf(mx1, __uint_as_float(sv[jj + 1]));
-            mx2 = fmaxf(mx2, __uint_as_float(sv[jj + 2]));
-            mx3 = fmaxf(mx3, __uint_as_float(sv[jj + 3]));
+          for (int jj = 0; jj < 64; jj += 8) {
+            mx0 = fmax3(mx0, __uint_as_float(sv[jj]), __uint_as_float(sv[jj + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(sv[jj + 2]), __uint_as_float(sv[jj + 3]));
+            mx2 = fmax3(mx2, __uint_as_float(sv[jj + 4]), __uint_as_float(sv[jj + 5]));
+            mx3 = fmax3(mx3, __uint_as_float(sv[jj + 6]), __uint_as_float(sv[jj + 7]));
           }
-          pm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+          pm = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;
         }
         if (ok) {
           // this warpgroup's own running maximum over its half of the keys
