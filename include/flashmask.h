@@ -99,8 +99,9 @@ typedef struct {
  * that want to read the classification. Regions marked [bwd] exist only when
  * the workspace was sized with for_bwd != 0 (otherwise their offsets are 0).
  *   status    int32[4]                   device status word (0 = OK; must be zero
- *                                        before first use, see above), detail, and the
- *                                        forward's work-item counter (reset by each call)
+ *                                        before first use, see above), detail, the
+ *                                        forward's work-item counter (reset by each
+ *                                        call) and the dQ-zeroed tag (see flashmask_fwd)
  *   minmax    int32  [B,Hm,Tc,8]         per key block: min/max of LTS, LTE, UTS, UTE
  *   labels    uint8  [B,Hm,Tr,Tc]        tile label, query-block major
  *   labels_t  uint8  [B,Hm,Tc,Tr]        tile label, key-block major
@@ -137,7 +138,12 @@ fm_status flashmask_classify(const fm_mask* mask, int B, int N, void* ws, size_t
 /* Forward: O [B,H,N,d] bf16 and LSE [B,H,N] fp32 from Q, K, V. `scale`
  * multiplies Q K^T (pass 1/sqrt(d) for standard attention). If
  * ws_classified == 0 the call runs flashmask_classify first; pass 1 to reuse a
- * classification of the same mask already in `ws`. Asynchronous on `stream`. */
+ * classification of the same mask already in `ws`. Asynchronous on `stream`.
+ * When ws_bytes is at least flashmask_workspace_bytes(..., for_bwd = 1), the
+ * forward also zeroes that layout's dQ accumulator (bulk copies issued while
+ * the attention runs) and leaves a tag of the shape in the fourth status word;
+ * the backward preprocess of the same shape on this workspace then skips its
+ * own zeroing pass, and the backward main kernel clears the tag again. */
 fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_mask* mask, int B,
                         int H, int N, int d, float scale, void* o, float* lse, void* ws,
                         size_t ws_bytes, int ws_classified, void* stream);
@@ -154,7 +160,9 @@ fm_status flashmask_bwd(const void* q, const void* k, const void* v, const void*
  * exposed so that a caller can schedule or time them separately. They must run
  * in this order on one stream with one workspace:
  *   preprocess: D = rowsum(dO * O), lse2 = LSE * log2(e), dQ accumulator = 0
- *               (HBM-bound; reads O and dO, writes 4*(2+d)*B*H*N bytes).
+ *               (HBM-bound; reads O and dO, writes 4*(2+d)*B*H*N bytes; the
+ *               accumulator's 4*d*B*H*N bytes are skipped when the preceding
+ *               flashmask_fwd on this workspace, of this shape, zeroed it).
  *   main:       dK, dV and the fp32 dQ accumulator over every non-FULL tile
  *               (needs a classification of `mask` and the preprocess output).
  *   finalize:   dQ = bf16(scale * accumulator).

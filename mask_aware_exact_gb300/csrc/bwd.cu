@@ -99,25 +99,15 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// all but the most recent bulk group have finished reading shared memory
-__device__ __forceinline__ void bulk_wait_read_1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 __device__ __forceinline__ void drain_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 
 // ---------------------------------------------------------------- preprocess
 // One padded row (bh, n) per D/8 threads, n < Npad: rows n >= N (the short last
-// block) get D = 0 and lse2 = +inf, so that their P is exactly 0.
+// block) get D = 0 and lse2 = +inf, so that their P is exactly 0. The dQ
+// accumulator row is zeroed too, unless the status word holds the tag that
+// the forward leaves after zeroing the accumulator of this same workspace
+// and problem shape itself.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                       const uint16_t* __restrict__ dout,
@@ -125,7 +115,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
                                                       float* __restrict__ delta,
                                                       float* __restrict__ lse2,
                                                       float* __restrict__ dq_accum,
-                                                      long long rows_pad, int N, int Npad) {
+                                                      long long rows_pad, int N, int Npad,
+                                                      const int32_t* zero_tag_word,
+                                                      int32_t zero_tag) {
   constexpr int kThreadsPerRow = D / 8;  // 8 bf16 (16 bytes) per thread
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long prow = gt / kThreadsPerRow;
@@ -146,7 +138,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
       acc = fmaf(__uint_as_float(ap[i] & 0xffff0000u), __uint_as_float(gp[i] & 0xffff0000u), acc);
     }
   }
-  if (prow < rows_pad) {
+  if (prow < rows_pad && *zero_tag_word != zero_tag) {
     float4* z = reinterpret_cast<float4*>(dq_accum + prow * D + part * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -183,6 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* list = p.col_list + (static_cast<size_t>(bm) * p.Tc + kb) * p.Tr;
   const int head_row0 = bh * p.N;
   const int k_row0 = head_row0 + kb * kTile;
+  // the accumulator is about to receive this backward's sums: a later
+  // preprocess must zero it again
+  if (blockIdx.x == 0 && tid == 0) p.status[3] = 0;
 
   if ((smem_u32(smem) & 1023u) != 0) {
     if (tid == 0) record_failure(p.status, kStatusLayout, kSiteBwdSmemAlign);
@@ -597,15 +592,17 @@ cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 
 cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
                            float* delta, float* lse2, float* dq_accum, long long heads, int N,
-                           int Npad, cudaStream_t s) {
+                           int Npad, const int32_t* zero_tag_word, int32_t zero_tag,
+                           cudaStream_t s) {
   const long long rows_pad = heads * Npad;
   const long long threads = rows_pad * (d / 8);
   const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
   if (d == 64)
-    bwd_pre_kernel<64><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows_pad, N, Npad);
+    bwd_pre_kernel<64><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows_pad, N, Npad,
+                                            zero_tag_word, zero_tag);
   else
     bwd_pre_kernel<128><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows_pad, N,
-                                             Npad);
+                                             Npad, zero_tag_word, zero_tag);
   return cudaGetLastError();
 }
 

@@ -70,6 +70,15 @@ fm_ws_layout make_layout(int B, int H, int Hm, int N, int d, int for_bwd) {
   return L;
 }
 
+// Nonzero tag of a backward workspace layout, left in the fourth status word by
+// a forward that zeroed the dQ accumulator of a workspace with this layout
+// (FNV-1a over the shape; bit 0 set so it is never 0).
+int32_t dq_zero_tag(int B, int H, int Hm, int N, int d) {
+  uint32_t h = 2166136261u;
+  for (int v : {B, H, Hm, N, d}) h = (h ^ static_cast<uint32_t>(v)) * 16777619u;
+  return static_cast<int32_t>(h | 1u);
+}
+
 fm::ClassifyTables tables(const fm_ws_layout& L, void* ws) {
   char* w = static_cast<char*>(ws);
   fm::ClassifyTables t;
@@ -293,6 +302,13 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
   p.sched = p.status + 2;  // third word of the 16-byte status region
   p.num_sms = sm_count();
   if (p.num_sms <= 0) return FM_ERR_CUDA;
+  // a workspace large enough for the backward gets its dQ accumulator zeroed
+  // here, where HBM is mostly idle, instead of in the backward preprocess
+  const fm_ws_layout Lb = make_layout(B, H, mask->Hm, N, d, 1);
+  p.dq_zero = ws_bytes >= Lb.total
+                  ? reinterpret_cast<float*>(static_cast<char*>(ws) + Lb.dq_accum)
+                  : nullptr;
+  p.dq_tag = dq_zero_tag(B, H, mask->Hm, N, d);
   return fm::launch_fwd(d, mq, mk, mv, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
@@ -370,6 +386,10 @@ fm_status flashmask_fwd_fp8(const void* q, const void* k, const void* v, const f
   p.sched = p.status + 2;
   p.num_sms = sm_count();
   if (p.num_sms <= 0) return FM_ERR_CUDA;
+  // the FP8 operands overlap a backward layout's dQ accumulator: the kernel
+  // clears the tag, so a later backward preprocess zeroes it again
+  p.dq_zero = nullptr;
+  p.dq_tag = 0;
   return fm::launch_fwd_fp8(mq, mk, mv, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
@@ -387,6 +407,8 @@ fm_status flashmask_bwd_preprocess(const void* o, const float* lse, const void* 
                             reinterpret_cast<float*>(w + L.lse2),
                             reinterpret_cast<float*>(w + L.dq_accum),
                             static_cast<long long>(B) * H, N, padded(N),
+                            reinterpret_cast<const int32_t*>(w + L.status) + 3,
+                            dq_zero_tag(B, H, Hm, N, d),
                             static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FM_OK
              : FM_ERR_CUDA;

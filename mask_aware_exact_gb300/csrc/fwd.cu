@@ -88,7 +88,11 @@ struct FwdLayout {
   static constexpr int kNumBars = 1 + kKSlots + kVSlots + 3 * kSRegions + 5;
   static constexpr int kSched = kBar + kNumBars * 8;  // int[4]
   static constexpr int kTmemSlot = kSched + 16;
-  static constexpr int kBytes = kTmemSlot + 16;
+  // 16 KB of zeros, the source of the bulk copies that clear the dQ
+  // accumulator rows of each query block (bf16 forward only)
+  static constexpr int kZero = kTmemSlot + 16;
+  static constexpr int kZeroBytes = kFp8 ? 0 : 16384;
+  static constexpr int kBytes = kZero + kZeroBytes;
 };
 
 struct FwdBars {
@@ -200,6 +204,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  if constexpr (!kFp8) {
+    if (p.dq_zero != nullptr) {
+      uint4* z = reinterpret_cast<uint4*>(smem + L::kZero);
+      for (int i = tid; i < L::kZeroBytes / 16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();  // the zeros are read by the bulk-copy engine
+    }
+  }
+  if (blockIdx.x == 0 && tid == 0) p.status[3] = p.dq_zero != nullptr ? p.dq_tag : 0;
   if (tid == 0) {
     mbar_init(bar.q_full(), 1);
     for (int s = 0; s < kKSlots; ++s) mbar_init(bar.k_full(s), 1);
@@ -285,6 +297,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       int J = 0, J_last = -1;  // running step; last step of the previous item with tiles
       for (int k = 0; ok && cur >= 0; ++k) {
         const Item it = decode(cur);
+        if constexpr (!kFp8) {
+          // zero this query block's rows of the backward's dQ accumulator
+          // (contiguous: 128 rows of D fp32) while the forward runs, which
+          // leaves HBM mostly idle, instead of in the backward preprocess
+          if (p.dq_zero != nullptr) {
+            char* dst = reinterpret_cast<char*>(
+                p.dq_zero + (static_cast<size_t>(it.bh) * p.Tr + it.r) * kTile * D);
+#pragma unroll
+            for (int c = 0; c < kTile * D * 4 / L::kZeroBytes; ++c)
+              bulk_store(dst + c * L::kZeroBytes, smem_u32(smem + L::kZero), L::kZeroBytes);
+            bulk_commit_group();
+            bulk_wait_read_8();
+          }
+        }
         if (it.ntiles > 0) {
           // the Q buffer is free once the last S of the previous item is done
           if (J_last >= 0 && !mbar_wait(bar.s_full(J_last % kSRegions),
@@ -313,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar.sched_full(s));
         cur = nxt;
       }
+      if constexpr (!kFp8) bulk_wait_all();  // the zeroing copies, before the CTA exits
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ TMA producer of V

@@ -70,6 +70,11 @@ struct FwdParams {
   int32_t* status;
   int32_t* sched;  // work-item counter (zeroed by the launch)
   int num_sms;     // persistent grid size
+  // Backward workspace only (else null): the fp32 dQ accumulator [B,H,Tr*128,d],
+  // whose rows of each query block the forward zeroes, and the tag it leaves in
+  // the fourth status word so that the backward preprocess can skip that pass.
+  float* dq_zero;
+  int32_t dq_tag;
 };
 
 struct BwdParams {
@@ -99,7 +104,8 @@ cudaError_t launch_quant_fp8(const uint16_t* q, const uint16_t* k, const uint16_
                              int N, const Fp8Operands& f, cudaStream_t s);
 cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
                            float* delta, float* lse2, float* dq_accum, long long heads, int N,
-                           int Npad, cudaStream_t s);
+                           int Npad, const int32_t* zero_tag_word, int32_t zero_tag,
+                           cudaStream_t s);
 cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
                        cudaStream_t s);
