@@ -1,8 +1,8 @@
-"""The forward zeroes the backward's fp32 dQ accumulator when its workspace is
+"""The dQ accumulator's life cycle. The forward zeroes it when its workspace is
 sized for the backward, and the backward preprocess of the same shape then
-skips that pass. Every case first fills the accumulator with NaN, so a zeroing
-that nobody did shows up as NaN or wrong dQ; dQ, dK and dV are compared with
-the fp64 oracle."""
+skips that pass. The cases fill the accumulator (and dQ) with NaN first, so a
+zeroing or a write that nobody did shows up as NaN or a wrong dQ; dQ, dK and
+dV are compared with the fp64 oracle."""
 import math
 
 import numpy as np
@@ -40,7 +40,8 @@ def _status_tag(ws):
 
 def _backward(fm, dev, o, lse, mask, ws):
     qd, kd, vd, dod = dev
-    dq, dk, dv = (torch.empty_like(qd) for _ in range(3))
+    dq = torch.full_like(qd, float("nan"))
+    dk, dv = (torch.empty_like(qd) for _ in range(2))
     fm.flashmask_bwd_preprocess(o, lse, dod, mask.Hm, ws)
     fm.flashmask_bwd_main(qd, kd, vd, dod, mask, ws, dk, dv)
     fm.flashmask_bwd_finalize(dq, mask.Hm, ws)
@@ -127,3 +128,21 @@ def test_fp8_forward_clears_the_tag():
     _poison_accumulator(fm, ws, mask.Hm)
     grads = _backward(fm, dev, o, lse, mask, ws)
     _check(host, spec, grads, "after an FP8 forward")
+
+
+def test_unseen_query_blocks_get_zero_dq():
+    # rows [256, 512) see no key at all: their query blocks (2 and 3) have no
+    # non-FULL tile, and their dQ must still come out exactly 0
+    fm = need_gpu()
+    lts = np.full((B, 1, N), 256, np.int32)
+    lte = np.full((B, 1, N), 512, np.int32)
+    spec = W.MaskSpec("causal_hole", True, lts, lte, None, None)
+    q, k, v, do = W.make_qkv(B, H, N, D, seed=8)
+    dev = [x.cuda() for x in (q, k, v, do)]
+    mask = fm.DeviceMask.from_spec(spec)
+    ws = fm.alloc_workspace(B, H, mask.Hm, N, D, for_bwd=True)
+    o, lse = fm.flashmask_fwd(dev[0], dev[1], dev[2], mask, ws)
+    grads = _backward(fm, dev, o, lse, mask, ws)
+    dq = to_np(grads[0])
+    assert np.all(dq[:, :, 256:512] == 0)
+    _check((q, k, v, do), spec, grads, "query blocks without visible keys")
