@@ -58,8 +58,8 @@ E2E_CHUNK_HEADS = 2
 # scaled by 4 to H = 32: every head is an independent unit of identical work,
 # so traffic grows in proportion to the heads.
 NCU_TRAFFIC = {
-    "bwd_main@6f64dc63d5fd@document_b1h32n32768d128": 4 * (405.986048e6 + 220.411392e6),
-    "fwd@f75aca89249c@document_b1h32n32768d128": 4 * (202.041088e6 + 49.646848e6),
+    "bwd_main@f9c4db247afa@document_b1h32n32768d128": 4 * (406.023680e6 + 221.003776e6),
+    "fwd@d66fe98bbfdc@document_b1h32n32768d128": 4 * (204.520704e6 + 164.038912e6),
 }
 
 

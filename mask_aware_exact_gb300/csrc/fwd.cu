@@ -297,20 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int J = 0, J_last = -1;  // running step; last step of the previous item with tiles
       for (int k = 0; ok && cur >= 0; ++k) {
         const Item it = decode(cur);
-        if constexpr (!kFp8) {
-          // zero this query block's rows of the backward's dQ accumulator
-          // (contiguous: 128 rows of D fp32) while the forward runs, which
-          // leaves HBM mostly idle, instead of in the backward preprocess
-          if (p.dq_zero != nullptr) {
-            char* dst = reinterpret_cast<char*>(
-                p.dq_zero + (static_cast<size_t>(it.bh) * p.Tr + it.r) * kTile * D);
-#pragma unroll
-            for (int c = 0; c < kTile * D * 4 / L::kZeroBytes; ++c)
-              bulk_store(dst + c * L::kZeroBytes, smem_u32(smem + L::kZero), L::kZeroBytes);
-            bulk_commit_group();
-            bulk_wait_read_8();
-          }
-        }
         if (it.ntiles > 0) {
           // the Q buffer is free once the last S of the previous item is done
           if (J_last >= 0 && !mbar_wait(bar.s_full(J_last % kSRegions),
@@ -325,6 +311,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; ok && j < it.ntiles; ++j, ++J)
             ok = load_k(J, it.list[j] >> 2, it.bh);
           J_last = J - 1;
+        }
+        if constexpr (!kFp8) {
+          // zero this query block's rows of the backward's dQ accumulator
+          // (contiguous: 128 rows of D fp32) while the forward runs, which
+          // leaves HBM mostly idle, instead of in the backward preprocess;
+          // issued after the item's Q and K loads so as not to delay them
+          if (p.dq_zero != nullptr) {
+            char* dst = reinterpret_cast<char*>(
+                p.dq_zero + (static_cast<size_t>(it.bh) * p.Tr + it.r) * kTile * D);
+#pragma unroll
+            for (int c = 0; c < kTile * D * 4 / L::kZeroBytes; ++c)
+              bulk_store(dst + c * L::kZeroBytes, smem_u32(smem + L::kZero), L::kZeroBytes);
+            bulk_commit_group();
+            bulk_wait_read_8();
+          }
         }
         // claim the next item once this one's loads are issued; its ring
         // entry was last used by item k - 1, which every reader has taken
