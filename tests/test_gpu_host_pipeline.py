@@ -30,6 +30,7 @@ CASES = [
     (1, 6, 3, 640, 128, (2, 6), "document"),
     (1, 2, 1, 256, 64, (1, 2), "workload0"),
     (2, 4, 1, 333, 128, (2,), "random"),
+    (1, 8, 1, 512, 64, (2, 4), "random"),
 ]
 
 
