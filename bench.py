@@ -58,8 +58,8 @@ E2E_CHUNK_HEADS = 2
 # scaled by 4 to H = 32: every head is an independent unit of identical work,
 # so traffic grows in proportion to the heads.
 NCU_TRAFFIC = {
-    "bwd_main@f9c4db247afa@document_b1h32n32768d128": 4 * (406.023680e6 + 221.003776e6),
-    "fwd@d66fe98bbfdc@document_b1h32n32768d128": 4 * (204.520704e6 + 164.038912e6),
+    "bwd_main@202fa8c25567@document_b1h32n32768d128": 4 * (406.023680e6 + 221.003776e6),
+    "fwd@196fd6b00911@document_b1h32n32768d128": 4 * (204.520704e6 + 164.038912e6),
 }
 
 
@@ -73,10 +73,16 @@ def peaks():
 
 
 def kernel_source_hash(files=("bwd.cu", "ptx.cuh")) -> str:
+    """Hash of the kernel sources' code: comments ("//" to the end of a line)
+    and surrounding whitespace are left out, so an edit of comments alone keeps
+    the hash (and the ncu traffic recorded for it)."""
     h = hashlib.sha1()
     for f in files:
-        with open(os.path.join(ROOT, "mask_aware_exact_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "mask_aware_exact_gb300", "csrc", f), encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:12]
 
 

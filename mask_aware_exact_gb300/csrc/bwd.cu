@@ -4,7 +4,9 @@
 // FlashAttention family):
 //
 //   bwd_pre     D_i = <dO_i, O_i> (fp32), lse2_i = LSE_i * log2(e) (+inf for a
-//               fully masked row, so its P is exactly 0), dQ accumulator = 0.
+//               fully masked row, so its P is exactly 0), dQ accumulator = 0
+//               (skipped when the forward of the same shape and workspace
+//               already zeroed it and left its tag in the status word).
 //   bwd_kernel  one CTA per (batch, head, key block of 128 keys), looping over
 //               the non-FULL query blocks of that key block:
 //                 S^T  = K Q^T              (tcgen05, TMEM)
@@ -19,7 +21,8 @@
 //               (Reductions issued as red.global from the drain warps were
 //               measured to slow the compute warps' exponentials and TMEM loads
 //               about 2.4x on GB300; the bulk reduce leaves that traffic to the
-//               TMA engine.)
+//               TMA engine. Either way one SM adds at most about 25 bytes per
+//               clock into L2, so a tile's 64 KB of dQ takes >= 2600 cycles.)
 //   dq_convert  dQ = bf16(scale * accumulator).
 //
 // Warp roles of bwd_kernel (448 threads): warps 0-7 compute, two warpgroups;

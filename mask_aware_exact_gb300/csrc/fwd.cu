@@ -19,6 +19,11 @@
 // in the epilogue: with m = max(m_0, m_1) and f_w = 2^(m_w - m),
 // O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1), the exact result.
 //
+// Given a workspace sized for the backward, the scheduler thread also zeroes
+// each query block's rows of the backward's fp32 dQ accumulator with bulk
+// copies from a zeroed shared-memory buffer, using HBM bandwidth the forward
+// leaves idle, and the backward preprocess then skips that pass.
+//
 // Persistent CTAs (one per SM) take query blocks from a work counter; see the
 // kernel's comment. Warp roles (384 threads):
 //   warps 0-7  softmax, two warpgroups. Thread (w, r) owns query row r (= TMEM
