@@ -115,10 +115,13 @@ typedef struct {
  *                                       row and for the padding rows n >= N)
  *   delta     fp32   [B,H,Npad]   [bwd]  rowsum(dO * O) (0 on padding rows)
  *   dq_accum  fp32   [B,H,Npad,d] [bwd]  dQ accumulator
- * with Tr = Tc = ceil(N / 128) and Npad = 128 * Tr. */
+ *   kv_part   fp32   [B,H,E,3,2,128,d] [bwd] dV, dK of the parts of a split key
+ *                                        block that finish first (see flashmask_bwd)
+ *   kv_sync   int32  [B,H,E,8]    [bwd]  arrivals and ready flags per split block
+ * with Tr = Tc = ceil(N / 128), Npad = 128 * Tr and E = min(Tc, 16). */
 typedef struct {
   size_t status, minmax, labels, labels_t, row_count, row_list, row_order, col_count, col_list,
-      col_order, lse2, delta, dq_accum, total;
+      col_order, lse2, delta, dq_accum, kv_part, kv_sync, total;
 } fm_ws_layout;
 
 /* Workspace size in bytes for the given problem; 0 for an unsupported shape. */
@@ -150,7 +153,13 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
 
 /* Backward: dQ, dK, dV [B,H,N,d] bf16 from Q, K, V, the forward's O and LSE,
  * and the upstream gradient dO. The workspace must be sized with for_bwd != 0.
- * ws_classified as in flashmask_fwd. Asynchronous on `stream`. */
+ * ws_classified as in flashmask_fwd. Asynchronous on `stream`. The main
+ * kernel gives each (head, key block) one CTA, except that with Tc >= 512 key
+ * blocks (the environment variable FM_BWD_SPLIT_MIN_BLOCKS changes 512), among
+ * the E = min(Tc, 16) longest key blocks of each head one seen by n query
+ * blocks is split over min(4, n / 64) CTAs when that is at least two (a
+ * global prefix would otherwise keep one SM busy long after the rest); the
+ * parts' fp32 dK, dV are added through the workspace. */
 fm_status flashmask_bwd(const void* q, const void* k, const void* v, const void* o,
                         const float* lse, const void* dout, const fm_mask* mask, int B, int H,
                         int N, int d, float scale, void* dq, void* dk, void* dv, void* ws,

@@ -103,6 +103,8 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
       : "memory");
 }
 __device__ __forceinline__ void drain_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// the 256 compute threads (warps 0-7)
+__device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 
 
 // ---------------------------------------------------------------- preprocess
@@ -120,9 +122,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
                                                       float* __restrict__ dq_accum,
                                                       long long rows_pad, int N, int Npad,
                                                       const int32_t* zero_tag_word,
-                                                      int32_t zero_tag) {
+                                                      int32_t zero_tag, int32_t* kv_sync,
+                                                      long long nsync) {
   constexpr int kThreadsPerRow = D / 8;  // 8 bf16 (16 bytes) per thread
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gt < nsync) kv_sync[gt] = 0;  // split key blocks' arrivals and flags
   const long long prow = gt / kThreadsPerRow;
   const int part = static_cast<int>(gt % kThreadsPerRow);
   const long long bh = prow / Npad;
@@ -157,7 +161,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
 }
 
 // ---------------------------------------------------------------- main
-template <int D>
+// kSplit: the grid has the split CTAs described below (p.split_e > 0); the
+// instantiation without them keeps the plain one-CTA-per-key-block code.
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -170,12 +176,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   // that run together reduce into one head's dQ accumulator, which then stays
   // in L2 (fp32 reductions into L2-resident lines run at about twice the rate
   // of reductions that reach DRAM).
-  const int bh = blockIdx.x / p.Tc, rank = blockIdx.x % p.Tc;
+  // Each head has Tc + E (kSplitParts - 1) CTAs: the first E kSplitParts
+  // take the E longest key blocks, kSplitParts slots each: a block seen by
+  // n query blocks is split into nparts = min(kSplitParts, n / kPartTiles)
+  // consecutive parts of its tile list when that is at least two (slots past
+  // nparts leave at once); the rest take the other key blocks whole. So a key
+  // block that every query block sees (a global prefix) does not keep one SM
+  // busy long after the others have finished.
+  const int E = kSplit ? p.split_e : 0;
+  const int per_head = p.Tc + E * (kSplitParts - 1);
+  const int bh = blockIdx.x / per_head, slot = blockIdx.x % per_head;
   const int b = bh / p.H, h = bh % p.H;
   const int bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
+  const bool cand = kSplit && slot < E * kSplitParts;
+  const int rank = cand ? slot / kSplitParts : slot - E * (kSplitParts - 1);
+  const int part = cand ? slot % kSplitParts : 0;
   const int kb = p.col_order[static_cast<size_t>(bm) * p.Tc + rank];
-  const int ntiles = p.col_count[static_cast<size_t>(bm) * p.Tc + kb];
-  const int32_t* list = p.col_list + (static_cast<size_t>(bm) * p.Tc + kb) * p.Tr;
+  const int count = p.col_count[static_cast<size_t>(bm) * p.Tc + kb];
+  const int nparts = cand ? min(kSplitParts, max(1, count / kPartTiles)) : 1;
+  if (kSplit && part >= nparts) return;  // this block needs fewer parts
+  const bool split = kSplit && nparts > 1;
+  const int t0 = part * count / nparts;
+  const int ntiles = (part + 1) * count / nparts - t0;
+  const int32_t* list = p.col_list + (static_cast<size_t>(bm) * p.Tc + kb) * p.Tr + t0;
   const int head_row0 = bh * p.N;
   const int k_row0 = head_row0 + kb * kTile;
   // the accumulator is about to receive this backward's sums: a later
@@ -472,8 +495,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = ok && ntiles > 0;
     uint16_t* dv_row = p.dv + static_cast<size_t>(k_row0 + j) * D + g * (D / 2);
     uint16_t* dk_row = p.dk + static_cast<size_t>(k_row0 + j) * D + g * (D / 2);
+    // a split key block: each part but the last to finish leaves its fp32
+    // dV, dK in the workspace slot of its arrival order; the last adds them
+    // to its own and writes the block
+    int add_parts = 0;
+    bool write_out = true;
+    float* part_base = nullptr;
+    if (split) {
+      int32_t* sync = p.kv_sync + (static_cast<size_t>(bh) * E + rank) * kSyncWords;
+      part_base = p.kv_part + (static_cast<size_t>(bh) * E + rank) * (kSplitParts - 1) * 2 * kTile * D;
+      volatile int* arrival_s = reinterpret_cast<volatile int*>(tmem_slot + 1);
+      if (tid == 0) *arrival_s = atomicAdd(sync, 1);
+      compute_bar();
+      const int arrival = *arrival_s;
+      if (arrival < nparts - 1) {
+        float* part = part_base + static_cast<size_t>(arrival) * 2 * kTile * D;
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t colbase = (which == 0 ? kColDV : kColDK) + g * (D / 2);
+#pragma unroll
+          for (int ch = 0; ch < D / 64; ++ch) {
+            uint32_t v[32];
+            if (live) {
+              tmem_ld32(tmem + lane_base + colbase + ch * 32, v);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = 0u;
+            }
+            float4* dst = reinterpret_cast<float4*>(part + (which * kTile + j) * D + g * (D / 2) +
+                                                    ch * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
+        }
+        __threadfence();
+        compute_bar();
+        if (tid == 0) atomicExch(sync + 1 + arrival, 1);  // this partial is complete
+        write_out = false;
+      } else {
+        // the other parts' partials: each has been counted, so it is being
+        // written by a CTA that waits for nothing; the waits are bounded all
+        // the same
+        if (tid == 0) {
+          const uint64_t w0 = global_timer_ns();
+          for (int i = 0; i < nparts - 1; ++i) {
+            while (*reinterpret_cast<volatile int32_t*>(sync + 1 + i) == 0) {
+              if (global_timer_ns() - w0 > FM_WAIT_LIMIT_NS) {
+                record_failure(p.status, kStatusTimeout, kSiteBwdSplit);
+                break;
+              }
+            }
+          }
+        }
+        compute_bar();
+        __threadfence();
+        add_parts = nparts - 1;
+      }
+    }
+#pragma unroll
+    for (int which = 0; which < 2 && write_out; ++which) {
       const uint32_t colbase = (which == 0 ? kColDV : kColDK) + g * (D / 2);
       const float f = which == 0 ? 1.f : p.scale;
       uint16_t* dst_row = which == 0 ? dv_row : dk_row;
@@ -485,6 +567,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        for (int q = 0; q < add_parts; ++q) {
+          const float4* src = reinterpret_cast<const float4*>(
+              part_base + static_cast<size_t>(q) * 2 * kTile * D + (which * kTile + j) * D +
+              g * (D / 2) + ch * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 a = __ldcg(src + i);
+            v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) + a.x);
+            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) + a.y);
+            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) + a.z);
+            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + a.w);
+          }
         }
         // every lane takes part in the (warp-collective) TMEM load; only
         // existing keys store
@@ -578,16 +673,17 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
   reinterpret_cast<uint4*>(dq)[i] = o;
 }
 
-template <int D>
+template <int D, bool kSplit>
 cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
                          cudaStream_t s) {
   using L = BwdLayout<D>;
-  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::kBytes);
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, kSplit>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(p.B * p.H * p.Tc);
-  bwd_kernel<D><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, mdo, mdq, p);
+  const int per_head = p.Tc + (kSplit ? p.split_e * (kSplitParts - 1) : 0);
+  const unsigned grid = static_cast<unsigned>(p.B * p.H * per_head);
+  bwd_kernel<D, kSplit><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, mdo, mdq, p);
   return cudaGetLastError();
 }
 
@@ -596,24 +692,29 @@ cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
                            float* delta, float* lse2, float* dq_accum, long long heads, int N,
                            int Npad, const int32_t* zero_tag_word, int32_t zero_tag,
-                           cudaStream_t s) {
+                           int32_t* kv_sync, int split_e, cudaStream_t s) {
   const long long rows_pad = heads * Npad;
   const long long threads = rows_pad * (d / 8);
   const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
+  const long long nsync = heads * split_e * kSyncWords;
   if (d == 64)
     bwd_pre_kernel<64><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows_pad, N, Npad,
-                                            zero_tag_word, zero_tag);
+                                            zero_tag_word, zero_tag, kv_sync, nsync);
   else
     bwd_pre_kernel<128><<<grid, 256, 0, s>>>(o, dout, lse, delta, lse2, dq_accum, rows_pad, N,
-                                             Npad, zero_tag_word, zero_tag);
+                                             Npad, zero_tag_word, zero_tag, kv_sync, nsync);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
                        cudaStream_t s) {
-  if (d == 64) return launch_bwd_t<64>(mq, mk, mv, mdo, mdq, p, s);
-  return launch_bwd_t<128>(mq, mk, mv, mdo, mdq, p, s);
+  const bool split = p.split_e > 0;
+  if (d == 64)
+    return split ? launch_bwd_t<64, true>(mq, mk, mv, mdo, mdq, p, s)
+                 : launch_bwd_t<64, false>(mq, mk, mv, mdo, mdq, p, s);
+  return split ? launch_bwd_t<128, true>(mq, mk, mv, mdo, mdq, p, s)
+               : launch_bwd_t<128, false>(mq, mk, mv, mdo, mdq, p, s);
 }
 
 cudaError_t launch_dq_convert(int d, const float* dq_accum, float scale, uint16_t* dq,

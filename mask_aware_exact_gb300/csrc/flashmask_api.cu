@@ -3,6 +3,7 @@
 // allocates device memory.
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -65,6 +66,12 @@ fm_ws_layout make_layout(int B, int H, int Hm, int N, int d, int for_bwd) {
     off = align_up(off + BHN * 4, 256);
     L.dq_accum = off;
     off = align_up(off + BHN * d * 4, 256);
+    const size_t E = fm::split_blocks(static_cast<int>(Tc));
+    L.kv_part = off;
+    off = align_up(off + static_cast<size_t>(B) * H * E * (fm::kSplitParts - 1) * 2 * kTile * d * 4,
+                   256);
+    L.kv_sync = off;
+    off = align_up(off + static_cast<size_t>(B) * H * E * fm::kSyncWords * 4, 256);
   }
   L.total = off;
   return L;
@@ -77,6 +84,15 @@ int32_t dq_zero_tag(int B, int H, int Hm, int N, int d) {
   uint32_t h = 2166136261u;
   for (int v : {B, H, Hm, N, d}) h = (h ^ static_cast<uint32_t>(v)) * 16777619u;
   return static_cast<int32_t>(h | 1u);
+}
+
+// The backward adds split CTAs only from this many key blocks per head on:
+// they cost an SM slot each even when no key block needs them (about 1% of
+// the backward at 256 key blocks), and only long sequences make key blocks
+// long enough to be worth splitting. FM_BWD_SPLIT_MIN_BLOCKS overrides it.
+int split_min_blocks() {
+  const char* e = std::getenv("FM_BWD_SPLIT_MIN_BLOCKS");
+  return e != nullptr ? std::atoi(e) : 512;
 }
 
 fm::ClassifyTables tables(const fm_ws_layout& L, void* ws) {
@@ -408,8 +424,9 @@ fm_status flashmask_bwd_preprocess(const void* o, const float* lse, const void* 
                             reinterpret_cast<float*>(w + L.dq_accum),
                             static_cast<long long>(B) * H, N, padded(N),
                             reinterpret_cast<const int32_t*>(w + L.status) + 3,
-                            dq_zero_tag(B, H, Hm, N, d),
-                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+                            dq_zero_tag(B, H, Hm, N, d), reinterpret_cast<int32_t*>(w + L.kv_sync),
+                            fm::split_blocks(blocks_of(N)), static_cast<cudaStream_t>(stream)) ==
+                     cudaSuccess
              ? FM_OK
              : FM_ERR_CUDA;
 }
@@ -452,6 +469,9 @@ fm_status flashmask_bwd_main(const void* q, const void* k, const void* v, const 
   p.lse2 = reinterpret_cast<float*>(w + L.lse2);
   p.delta = reinterpret_cast<float*>(w + L.delta);
   p.dq_accum = dq_accum;
+  p.split_e = p.Tc >= split_min_blocks() ? fm::split_blocks(p.Tc) : 0;
+  p.kv_part = reinterpret_cast<float*>(w + L.kv_part);
+  p.kv_sync = reinterpret_cast<int32_t*>(w + L.kv_sync);
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
   p.status = reinterpret_cast<int32_t*>(w + L.status);

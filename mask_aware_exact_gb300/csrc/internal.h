@@ -17,9 +17,18 @@ enum Site : int {
   kSiteFwdQ = 101, kSiteFwdK, kSiteFwdV, kSiteFwdS, kSiteFwdP, kSiteFwdO, kSiteFwdKEmpty,
   kSiteFwdVEmpty, kSiteFwdSmemAlign, kSiteFwdSched,
   kSiteBwdKV = 201, kSiteBwdQ, kSiteBwdQEmpty, kSiteBwdS, kSiteBwdDP, kSiteBwdPT, kSiteBwdDS,
-  kSiteBwdDV, kSiteBwdDQ, kSiteBwdDrained, kSiteBwdDone, kSiteBwdSmemAlign,
+  kSiteBwdDV, kSiteBwdDQ, kSiteBwdDrained, kSiteBwdDone, kSiteBwdSmemAlign, kSiteBwdSplit,
   kSiteSelftest = 301,
 };
+
+// Backward load balance: among the split_blocks(Tc) longest key blocks of
+// each head, one seen by n query blocks is processed by min(kSplitParts,
+// n / kPartTiles) CTAs (consecutive parts of its tile list) when that is at
+// least two; the parts add their dK, dV through kv_part.
+constexpr int kSplitParts = 4;
+constexpr int kPartTiles = 64;
+constexpr int kSyncWords = 8;  // per split block: arrivals, ready flags of the parts
+__host__ __device__ constexpr int split_blocks(int Tc) { return Tc < 16 ? Tc : 16; }
 
 struct MaskDev {
   const int32_t* lts;
@@ -89,6 +98,12 @@ struct BwdParams {
   const float* lse2;   // [B,H,Npad]
   const float* delta;  // [B,H,Npad]
   float* dq_accum;     // [B,H,Npad,d]
+  // The E = split_blocks(Tc) longest key blocks of each head may be split
+  // over up to kSplitParts CTAs; all parts but the last to finish leave their
+  // fp32 dV, dK in kv_part (slot = arrival order), the last adds them.
+  int split_e;
+  float* kv_part;      // [B,H,E,kSplitParts-1,2,128,d]
+  int32_t* kv_sync;    // [B,H,E,kSyncWords]: arrivals, then one ready flag per slot
   uint16_t* dk;
   uint16_t* dv;
   int32_t* status;
@@ -105,7 +120,7 @@ cudaError_t launch_quant_fp8(const uint16_t* q, const uint16_t* k, const uint16_
 cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
                            float* delta, float* lse2, float* dq_accum, long long heads, int N,
                            int Npad, const int32_t* zero_tag_word, int32_t zero_tag,
-                           cudaStream_t s);
+                           int32_t* kv_sync, int split_e, cudaStream_t s);
 cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
                        cudaStream_t s);

@@ -33,7 +33,8 @@ class _FmMask(ctypes.Structure):
 class FmWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "minmax", "labels", "labels_t", "row_count", "row_list", "row_order",
-                 "col_count", "col_list", "col_order", "lse2", "delta", "dq_accum", "total")]
+                 "col_count", "col_list", "col_order", "lse2", "delta", "dq_accum", "kv_part",
+                 "kv_sync", "total")]
 
 
 class FmFp8Layout(ctypes.Structure):

@@ -55,19 +55,24 @@ def test_workspace_sizes(lib):
     # a sequence length that is not a multiple of 128: the tables cover
     # ceil(N / 128) blocks and the backward arrays are padded to 128 rows
     L = fm.flashmask_workspace_layout(1, 2, 1, 1000, 64, True)
-    assert L.total - L.dq_accum == 2 * 1024 * 64 * 4
+    assert L.kv_part - L.dq_accum == 2 * 1024 * 64 * 4
+    # split key blocks: E = min(Tc, 16) = 8 per head, three parts' fp32 dV, dK rows
+    assert L.kv_sync - L.kv_part == 2 * 8 * 3 * 2 * 128 * 64 * 4
+    assert L.total - L.kv_sync == 2 * 8 * 8 * 4  # 8 int32 per split block
     assert L.labels_t - L.labels >= 8 * 8
 
 
 def test_workspace_layout_regions_disjoint(lib):
     L = fm.flashmask_workspace_layout(2, 8, 2, 1024, 64, True)
     offs = [L.status, L.minmax, L.labels, L.labels_t, L.row_count, L.row_list, L.row_order,
-            L.col_count, L.col_list, L.col_order, L.lse2, L.delta, L.dq_accum, L.total]
+            L.col_count, L.col_list, L.col_order, L.lse2, L.delta, L.dq_accum, L.kv_part,
+            L.kv_sync, L.total]
     assert offs == sorted(offs) and len(set(offs)) == len(offs)
     assert all(o % 256 == 0 for o in offs)
     Tr = 1024 // 128
     assert L.labels_t - L.labels >= 2 * 2 * Tr * Tr
-    assert L.total - L.dq_accum == 2 * 8 * 1024 * 64 * 4
+    assert L.kv_part - L.dq_accum == 2 * 8 * 1024 * 64 * 4
+    assert L.kv_sync - L.kv_part == 2 * 8 * 8 * 3 * 2 * 128 * 64 * 4
 
 
 FAKE = 1 << 20  # a 256-aligned non-null address; validation fails before it is used

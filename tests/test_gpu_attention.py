@@ -197,6 +197,20 @@ def test_window_prefix_reduced_full():
     full_compare(fm, q, k, v, do, spec, what="window_prefix N=8192")
 
 
+@pytest.mark.parametrize("N,d", [(16384, 128), (16347, 64), (32768, 64)])
+def test_split_key_blocks_full(N, d, monkeypatch):
+    # a 512-token global prefix: its four key blocks are seen by every query
+    # block (128 of them at 16K, 256 at 32K), so the backward (splitting from
+    # 0 key blocks on here, 512 by default) splits each over two (16K) or four
+    # (32K) CTAs and adds the parts' dK, dV; compared in full with the oracle
+    monkeypatch.setenv("FM_BWD_SPLIT_MIN_BLOCKS", "0")
+    fm = need_gpu()
+    B, H = 1, 1
+    spec = W.window_prefix_bounds(B, 1, N, 1024, 512)
+    q, k, v, do = W.make_qkv(B, H, N, d, seed=21)
+    full_compare(fm, q, k, v, do, spec, what=f"split key blocks N={N} d={d}")
+
+
 @pytest.mark.parametrize("N,d,kind", [(129, 64, "causal"), (200, 128, "document"),
                                       (333, 64, "random"), (600, 128, "window_prefix"),
                                       (1000, 128, "share_question"), (77, 128, "random")])
