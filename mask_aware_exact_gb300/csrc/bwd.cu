@@ -124,39 +124,55 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
                                                       const int32_t* zero_tag_word,
                                                       int32_t zero_tag, int32_t* kv_sync,
                                                       long long nsync) {
-  constexpr int kThreadsPerRow = D / 8;  // 8 bf16 (16 bytes) per thread
+  constexpr int kThreadsPerRow = D / 8;  // 8 bf16 (16 bytes) per thread and row
+  constexpr int kRows = 4;               // rows per thread, their loads all in flight
   const long long gt = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gt < nsync) kv_sync[gt] = 0;  // split key blocks' arrivals and flags
-  const long long prow = gt / kThreadsPerRow;
   const int part = static_cast<int>(gt % kThreadsPerRow);
-  const long long bh = prow / Npad;
-  const int n = static_cast<int>(prow - bh * Npad);
-  const bool live = prow < rows_pad && n < N;
-  const long long row = bh * N + n;  // row of O, dO and LSE
-  float acc = 0.f;
-  if (live) {
-    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
-    const uint4 g = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
-    const uint32_t* ap = reinterpret_cast<const uint32_t*>(&a);
-    const uint32_t* gp = reinterpret_cast<const uint32_t*>(&g);
+  const long long prow0 = (gt / kThreadsPerRow / 2) * (2 * kRows) + (gt / kThreadsPerRow) % 2;
+  const bool zero_acc = *zero_tag_word != zero_tag;
+  // rows prow0 + 2r (r < kRows): a warp's two row groups interleave, so each
+  // load instruction reads two whole 2d-byte rows
+  uint4 a[kRows], g[kRows];
+  float L[kRows];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const long long prow = prow0 + 2 * r;
+    const long long bh = prow / Npad;
+    const int n = static_cast<int>(prow - bh * Npad);
+    const bool live = prow < rows_pad && n < N;
+    const long long row = bh * N + n;  // row of O, dO and LSE
+    a[r] = g[r] = make_uint4(0u, 0u, 0u, 0u);
+    L[r] = -INFINITY;
+    if (live) {
+      a[r] = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
+      g[r] = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
+      if (part == 0) L[r] = lse[row];
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const long long prow = prow0 + 2 * r;
+    float acc = 0.f;
+    const uint32_t* ap = reinterpret_cast<const uint32_t*>(&a[r]);
+    const uint32_t* gp = reinterpret_cast<const uint32_t*>(&g[r]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       acc = fmaf(__uint_as_float(ap[i] << 16), __uint_as_float(gp[i] << 16), acc);
       acc = fmaf(__uint_as_float(ap[i] & 0xffff0000u), __uint_as_float(gp[i] & 0xffff0000u), acc);
     }
-  }
-  if (prow < rows_pad && *zero_tag_word != zero_tag) {
-    float4* z = reinterpret_cast<float4*>(dq_accum + prow * D + part * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+    if (prow < rows_pad && zero_acc) {
+      float4* z = reinterpret_cast<float4*>(dq_accum + prow * D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
-  for (int off = kThreadsPerRow / 2; off > 0; off >>= 1)
-    acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (prow < rows_pad && part == 0) {
-    delta[prow] = acc;
-    const float L = live ? lse[row] : -INFINITY;
-    lse2[prow] = (L == -INFINITY) ? INFINITY : L * 1.4426950408889634f;
+    for (int off = kThreadsPerRow / 2; off > 0; off >>= 1)
+      acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (prow < rows_pad && part == 0) {
+      delta[prow] = acc;
+      lse2[prow] = (L[r] == -INFINITY) ? INFINITY : L[r] * 1.4426950408889634f;
+    }
   }
 }
 
@@ -694,7 +710,7 @@ cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const
                            int Npad, const int32_t* zero_tag_word, int32_t zero_tag,
                            int32_t* kv_sync, int split_e, cudaStream_t s) {
   const long long rows_pad = heads * Npad;
-  const long long threads = rows_pad * (d / 8);
+  const long long threads = rows_pad * (d / 8) / 4;  // four rows per thread
   const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
   const long long nsync = heads * split_e * kSyncWords;
   if (d == 64)
