@@ -102,6 +102,17 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
+// 3-D tiled store of one box from shared memory (x, y, z = column, row within
+// the head, head), in the current bulk async-group; rows outside the tensor map
+// are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
 __device__ __forceinline__ void drain_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 // the 256 compute threads (warps 0-7)
 __device__ __forceinline__ void compute_bar() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
@@ -183,7 +194,8 @@ template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-               const __grid_constant__ CUtensorMap mdq, const BwdParams p) {
+               const __grid_constant__ CUtensorMap mdq, const __grid_constant__ CUtensorMap mdk,
+               const __grid_constant__ CUtensorMap mdv, const BwdParams p) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -215,8 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t0 = part * count / nparts;
   const int ntiles = (part + 1) * count / nparts - t0;
   const int32_t* list = p.col_list + (static_cast<size_t>(bm) * p.Tc + kb) * p.Tr + t0;
-  const int head_row0 = bh * p.N;
-  const int k_row0 = head_row0 + kb * kTile;
   // the accumulator is about to receive this backward's sums: a later
   // preprocess must zero it again
   if (blockIdx.x == 0 && tid == 0) p.status[3] = 0;
@@ -509,8 +519,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     const bool live = ok && ntiles > 0;
-    uint16_t* dv_row = p.dv + static_cast<size_t>(k_row0 + j) * D + g * (D / 2);
-    uint16_t* dk_row = p.dk + static_cast<size_t>(k_row0 + j) * D + g * (D / 2);
     // a split key block: each part but the last to finish leaves its fp32
     // dV, dK in the workspace slot of its arrival order; the last adds them
     // to its own and writes the block
@@ -570,11 +578,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         add_parts = nparts - 1;
       }
     }
-#pragma unroll
+    // dV, then dK (scaled), as bf16 through the dS^T buffer (free once the
+    // last tile's products have completed) and TMA stores of 64-column boxes;
+    // keys >= N of a short last key block lie outside the tensor maps and are
+    // not written. Thread (g, j) writes row j, columns [g D/2, g D/2 + D/2):
+    // half g of the buffer for d = 128, 16-byte units [4g, 4g + 4) of its
+    // single box for d = 64.
+    const bool store_thread = tid == 0;
     for (int which = 0; which < 2 && write_out; ++which) {
       const uint32_t colbase = (which == 0 ? kColDV : kColDK) + g * (D / 2);
       const float f = which == 0 ? 1.f : p.scale;
-      uint16_t* dst_row = which == 0 ? dv_row : dk_row;
+      if (which == 1) {
+        if (store_thread) bulk_wait_read_all();  // the dV boxes have been read
+        compute_bar();
+      }
 #pragma unroll
       for (int ch = 0; ch < D / 64; ++ch) {
         uint32_t v[32];
@@ -597,11 +614,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) + a.w);
           }
         }
-        // every lane takes part in the (warp-collective) TMEM load; only
-        // existing keys store
-        if (key_exists) store_row32_bf16(dst_row + ch * 32, v, f);
+        uint32_t w16[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w16[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * f, __uint_as_float(v[2 * i + 1]) * f);
+        const uint32_t half = D == 128 ? sDS + g * 16384 : sDS;
+        const int unit0 = D == 128 ? 4 * ch : 4 * g;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(half + sw128_offset(j, unit0 + u), w16[4 * u], w16[4 * u + 1],
+                       w16[4 * u + 2], w16[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      compute_bar();
+      if (store_thread) {
+#pragma unroll
+        for (int box = 0; box < D / 64; ++box)
+          tma_store_3d(which == 0 ? &mdv : &mdk, sDS + box * 16384, 64 * box, kb * kTile, bh);
+        bulk_commit_group();
       }
     }
+    if (store_thread) bulk_wait_read_all();  // before the CTA's shared memory goes
   } else {
     // ------------------------------------------------------------ dQ drain
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -657,7 +690,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t + 2 < ntiles) mbar_arrive(bar.do_empty(st));
       }
     }
-    if (leader) bulk_wait_all();
+    // the last reductions must have read their boxes before the CTA's
+    // shared memory goes; their adds complete before the kernel does
+    if (leader) bulk_wait_read_all();
   }
 
   tc_fence_before();
@@ -691,7 +726,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 
 template <int D, bool kSplit>
 cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
+                         const CUtensorMap& mdo, const CUtensorMap& mdq, const CUtensorMap& mdk,
+                         const CUtensorMap& mdv, const BwdParams& p,
                          cudaStream_t s) {
   using L = BwdLayout<D>;
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, kSplit>,
@@ -699,7 +735,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   if (e != cudaSuccess) return e;
   const int per_head = p.Tc + (kSplit ? p.split_e * (kSplitParts - 1) : 0);
   const unsigned grid = static_cast<unsigned>(p.B * p.H * per_head);
-  bwd_kernel<D, kSplit><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, mdo, mdq, p);
+  bwd_kernel<D, kSplit><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, mdo, mdq, mdk, mdv, p);
   return cudaGetLastError();
 }
 
@@ -723,14 +759,15 @@ cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const
 }
 
 cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
+                       const CUtensorMap& mdo, const CUtensorMap& mdq, const CUtensorMap& mdk,
+                       const CUtensorMap& mdv, const BwdParams& p,
                        cudaStream_t s) {
   const bool split = p.split_e > 0;
   if (d == 64)
-    return split ? launch_bwd_t<64, true>(mq, mk, mv, mdo, mdq, p, s)
-                 : launch_bwd_t<64, false>(mq, mk, mv, mdo, mdq, p, s);
-  return split ? launch_bwd_t<128, true>(mq, mk, mv, mdo, mdq, p, s)
-               : launch_bwd_t<128, false>(mq, mk, mv, mdo, mdq, p, s);
+    return split ? launch_bwd_t<64, true>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s)
+                 : launch_bwd_t<64, false>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s);
+  return split ? launch_bwd_t<128, true>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s)
+               : launch_bwd_t<128, false>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s);
 }
 
 cudaError_t launch_dq_convert(int d, const float* dq_accum, float scale, uint16_t* dq,

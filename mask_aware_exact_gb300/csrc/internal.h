@@ -122,7 +122,8 @@ cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const
                            int Npad, const int32_t* zero_tag_word, int32_t zero_tag,
                            int32_t* kv_sync, int split_e, cudaStream_t s);
 cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
+                       const CUtensorMap& mdo, const CUtensorMap& mdq, const CUtensorMap& mdk,
+                       const CUtensorMap& mdv, const BwdParams& p,
                        cudaStream_t s);
 cudaError_t launch_dq_convert(int d, const float* dq_accum, float scale, uint16_t* dq,
                               long long heads, int N, int Npad, cudaStream_t s);
