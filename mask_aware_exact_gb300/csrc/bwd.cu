@@ -102,16 +102,9 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
       "r"(x), "r"(y), "r"(src)
       : "memory");
 }
-// 3-D tiled store of one box from shared memory (x, y, z = column, row within
-// the head, head), in the current bulk async-group; rows outside the tensor map
-// are not written.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
-                                             int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(x), "r"(y), "r"(z), "r"(src)
-      : "memory");
+// Prefetch of `bytes` (a multiple of 16) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void drain_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 // the 256 compute threads (warps 0-7)
@@ -194,8 +187,7 @@ template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-               const __grid_constant__ CUtensorMap mdq, const __grid_constant__ CUtensorMap mdk,
-               const __grid_constant__ CUtensorMap mdv, const BwdParams p) {
+               const __grid_constant__ CUtensorMap mdq, const BwdParams p) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -213,12 +205,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // busy long after the others have finished.
   const int E = kSplit ? p.split_e : 0;
   const int per_head = p.Tc + E * (kSplitParts - 1);
-  const int bh = blockIdx.x / per_head, slot = blockIdx.x % per_head;
-  const int b = bh / p.H, h = bh % p.H;
-  const int bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
-  const bool cand = kSplit && slot < E * kSplitParts;
-  const int rank = cand ? slot / kSplitParts : slot - E * (kSplitParts - 1);
-  const int part = cand ? slot % kSplitParts : 0;
+  // head, mask head, rank and part of CTA `idx`
+  auto decode = [&](int idx, int& bh_, int& bm_, int& rank_, int& part_, bool& cand_) {
+    bh_ = idx / per_head;
+    const int slot = idx % per_head;
+    const int b_ = bh_ / p.H, h_ = bh_ % p.H;
+    bm_ = b_ * p.mask.Hm + h_ / (p.H / p.mask.Hm);
+    cand_ = kSplit && slot < E * kSplitParts;
+    rank_ = cand_ ? slot / kSplitParts : slot - E * (kSplitParts - 1);
+    part_ = cand_ ? slot % kSplitParts : 0;
+  };
+  int bh, bm, rank, part;
+  bool cand;
+  decode(blockIdx.x, bh, bm, rank, part, cand);
   const int kb = p.col_order[static_cast<size_t>(bm) * p.Tc + rank];
   const int count = p.col_count[static_cast<size_t>(bm) * p.Tc + kb];
   const int nparts = cand ? min(kSplitParts, max(1, count / kPartTiles)) : 1;
@@ -243,16 +242,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   const BwdBars bar{smem_u32(smem + L::kBar)};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
+  // Q and lse2 (which = 0) or dO and D (which = 1) of tile t into stage t % 2;
+  // lse2 and D live in the padded [B*H, Npad] workspace arrays
+  auto load_tile = [&](int t, int which) {
+    const int st = t & 1;
+    const int qb = list[t] >> 2;
+    const size_t prow = static_cast<size_t>(bh) * p.Npad + qb * kTile;
+    const uint32_t fb = which == 0 ? bar.q_full(st) : bar.do_full(st);
+    const uint32_t dst = (which == 0 ? sQ : sDO) + st * L::kTileBytes;
+    mbar_arrive_expect_tx(fb, L::kTileBytes + kTile * 4);
+    for (int ch = 0; ch < L::kChunks; ++ch)
+      tma_load_3d(dst + ch * 16384, which == 0 ? &mq : &mdo, ch * 64, qb * kTile, bh, fb);
+    bulk_load(smem_u32((which == 0 ? lse_s : delta_s) + st * kTile),
+              (which == 0 ? p.lse2 : p.delta) + prow, kTile * 4, fb);
+  };
+  if (warp == 12 && lane == 0) {
+    // The producer sets up the barriers its loads complete and issues K, V
+    // and the first two tiles before the block-wide sync, so that the loads
+    // overlap the TMEM allocation and the other set-up.
+    mbar_init(bar.kv_full(), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar.q_full(s), 1);
+      mbar_init(bar.do_full(s), 1);
+    }
+    fence_barrier_init();
+    if (ntiles > 0) {
+      tma_prefetch_desc(&mq);
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+      tma_prefetch_desc(&mdo);
+      mbar_arrive_expect_tx(bar.kv_full(), 2 * L::kTileBytes);
+      for (int ch = 0; ch < L::kChunks; ++ch) {
+        tma_load_3d(sK + ch * 16384, &mk, ch * 64, kb * kTile, bh, bar.kv_full());
+        tma_load_3d(sV + ch * 16384, &mv, ch * 64, kb * kTile, bh, bar.kv_full());
+      }
+      for (int t = 0; t < 2 && t < ntiles; ++t) {
+        load_tile(t, 0);
+        load_tile(t, 1);
+      }
+    }
+  }
   if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(bar.kv_full(), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar.q_full(s), 1);
       mbar_init(bar.q_empty(s), 1);
-      mbar_init(bar.do_full(s), 1);
       mbar_init(bar.do_empty(s), 1);
     }
     mbar_init(bar.s_full(), 1);
@@ -272,42 +308,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 12) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && ntiles > 0) {
-      tma_prefetch_desc(&mq);
-      tma_prefetch_desc(&mk);
-      tma_prefetch_desc(&mv);
-      tma_prefetch_desc(&mdo);
-      mbar_arrive_expect_tx(bar.kv_full(), 2 * L::kTileBytes);
-      for (int ch = 0; ch < L::kChunks; ++ch) {
-        tma_load_3d(sK + ch * 16384, &mk, ch * 64, kb * kTile, bh, bar.kv_full());
-        tma_load_3d(sV + ch * 16384, &mv, ch * 64, kb * kTile, bh, bar.kv_full());
+      // K and V of the CTA that will start about one CTA duration from now
+      // (CTAs start in index order, one per SM) go to L2 ahead of its own
+      // loads, which then do not wait for DRAM
+      const int fut = blockIdx.x + p.num_sms;
+      if (fut < static_cast<int>(gridDim.x)) {
+        int fbh, fbm, frank, fpart;
+        bool fcand;
+        decode(fut, fbh, fbm, frank, fpart, fcand);
+        const int fkb = p.col_order[static_cast<size_t>(fbm) * p.Tc + frank];
+        const int rows = min(kTile, p.N - fkb * kTile);
+        const size_t off = (static_cast<size_t>(fbh) * p.N + fkb * kTile) * D;
+        bulk_prefetch_l2(p.k + off, rows * D * 2);
+        bulk_prefetch_l2(p.v + off, rows * D * 2);
       }
-      for (int t = 0; t < ntiles; ++t) {
+      for (int t = 2; t < ntiles; ++t) {
         const int st = t & 1;
-        const int q_row = (list[t] >> 2) * kTile;  // first row of the query block in its head
-        // lse2 and D live in the padded [B*H, Npad] workspace arrays
-        const size_t prow = static_cast<size_t>(bh) * p.Npad + (list[t] >> 2) * kTile;
-        // Q and lse2 of stage st (freed once the dQ boxes staged in the Q
-        // buffer two tiles earlier have been read by the bulk reduce) ...
-        if (t >= 2 && !mbar_wait(bar.q_empty(st), ((t >> 1) - 1) & 1, p.status)) {
+        // the Q (then dO) buffer of stage st is free once the dQ boxes staged
+        // in it two tiles earlier have been read by the bulk reduce; Q goes
+        // first, so that S and P of a tile can start before its dO lands
+        if (!mbar_wait(bar.q_empty(st), ((t >> 1) - 1) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteBwdQEmpty);
           break;
         }
-        mbar_arrive_expect_tx(bar.q_full(st), L::kTileBytes + kTile * 4);
-        for (int ch = 0; ch < L::kChunks; ++ch)
-          tma_load_3d(sQ + st * L::kTileBytes + ch * 16384, &mq, ch * 64, q_row, bh,
-                      bar.q_full(st));
-        bulk_load(smem_u32(lse_s + st * kTile), p.lse2 + prow, kTile * 4, bar.q_full(st));
-        // ... then dO and D (freed when the boxes staged in the dO buffer have
-        // been read), so that S and P of a tile can start before its dO lands
-        if (t >= 2 && !mbar_wait(bar.do_empty(st), ((t >> 1) - 1) & 1, p.status)) {
+        load_tile(t, 0);
+        if (!mbar_wait(bar.do_empty(st), ((t >> 1) - 1) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteBwdQEmpty);
           break;
         }
-        mbar_arrive_expect_tx(bar.do_full(st), L::kTileBytes + kTile * 4);
-        for (int ch = 0; ch < L::kChunks; ++ch)
-          tma_load_3d(sDO + st * L::kTileBytes + ch * 16384, &mdo, ch * 64, q_row, bh,
-                      bar.do_full(st));
-        bulk_load(smem_u32(delta_s + st * kTile), p.delta + prow, kTile * 4, bar.do_full(st));
+        load_tile(t, 1);
       }
     }
   } else if (warp == 13) {
@@ -579,19 +608,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // dV, then dK (scaled), as bf16 through the dS^T buffer (free once the
-    // last tile's products have completed) and TMA stores of 64-column boxes;
-    // keys >= N of a short last key block lie outside the tensor maps and are
-    // not written. Thread (g, j) writes row j, columns [g D/2, g D/2 + D/2):
-    // half g of the buffer for d = 128, 16-byte units [4g, 4g + 4) of its
-    // single box for d = 64.
-    const bool store_thread = tid == 0;
+    // last tile's products have completed): thread (g, j) writes row j,
+    // columns [g D/2, g D/2 + D/2), into the buffer (128-byte swizzled rows:
+    // half g for d = 128, 16-byte units [4g, 4g + 4) of a single half for
+    // d = 64); then the 256 threads copy the tile out in 16-byte pieces, a
+    // warp covering whole consecutive rows, so that every store is
+    // coalesced. Keys >= N of a short last key block are not written.
+    constexpr int kRowPieces = D / 8;  // 16-byte pieces per row
     for (int which = 0; which < 2 && write_out; ++which) {
       const uint32_t colbase = (which == 0 ? kColDV : kColDK) + g * (D / 2);
       const float f = which == 0 ? 1.f : p.scale;
-      if (which == 1) {
-        if (store_thread) bulk_wait_read_all();  // the dV boxes have been read
-        compute_bar();
-      }
+      if (which == 1) compute_bar();  // the dV tile has been copied out
 #pragma unroll
       for (int ch = 0; ch < D / 64; ++ch) {
         uint32_t v[32];
@@ -625,16 +652,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_shared_v4(half + sw128_offset(j, unit0 + u), w16[4 * u], w16[4 * u + 1],
                        w16[4 * u + 2], w16[4 * u + 3]);
       }
-      fence_proxy_async_smem();
       compute_bar();
-      if (store_thread) {
+      uint16_t* out = (which == 0 ? p.dv : p.dk) + (static_cast<size_t>(bh) * p.N + kb * kTile) * D;
 #pragma unroll
-        for (int box = 0; box < D / 64; ++box)
-          tma_store_3d(which == 0 ? &mdv : &mdk, sDS + box * 16384, 64 * box, kb * kTile, bh);
-        bulk_commit_group();
+      for (int i = 0; i < kTile * kRowPieces / 256; ++i) {
+        const int c = tid + 256 * i;  // piece c: row c / kRowPieces, piece c % kRowPieces
+        const int row = c / kRowPieces, pc = c % kRowPieces;
+        const uint32_t src = D == 128 ? sDS + (pc >> 3) * 16384 + sw128_offset(row, pc & 7)
+                                      : sDS + sw128_offset(row, pc);
+        uint32_t a0, a1, a2, a3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                     : "r"(src)
+                     : "memory");
+        if (kb * kTile + row < p.N)
+          *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * D + pc * 8) =
+              make_uint4(a0, a1, a2, a3);
       }
     }
-    if (store_thread) bulk_wait_read_all();  // before the CTA's shared memory goes
   } else {
     // ------------------------------------------------------------ dQ drain
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -726,8 +761,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 
 template <int D, bool kSplit>
 cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, const CUtensorMap& mdq, const CUtensorMap& mdk,
-                         const CUtensorMap& mdv, const BwdParams& p,
+                         const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
                          cudaStream_t s) {
   using L = BwdLayout<D>;
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<D, kSplit>,
@@ -735,7 +769,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   if (e != cudaSuccess) return e;
   const int per_head = p.Tc + (kSplit ? p.split_e * (kSplitParts - 1) : 0);
   const unsigned grid = static_cast<unsigned>(p.B * p.H * per_head);
-  bwd_kernel<D, kSplit><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, mdo, mdq, mdk, mdv, p);
+  bwd_kernel<D, kSplit><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, mdo, mdq, p);
   return cudaGetLastError();
 }
 
@@ -759,15 +793,14 @@ cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const
 }
 
 cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const CUtensorMap& mdo, const CUtensorMap& mdq, const CUtensorMap& mdk,
-                       const CUtensorMap& mdv, const BwdParams& p,
+                       const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
                        cudaStream_t s) {
   const bool split = p.split_e > 0;
   if (d == 64)
-    return split ? launch_bwd_t<64, true>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s)
-                 : launch_bwd_t<64, false>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s);
-  return split ? launch_bwd_t<128, true>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s)
-               : launch_bwd_t<128, false>(mq, mk, mv, mdo, mdq, mdk, mdv, p, s);
+    return split ? launch_bwd_t<64, true>(mq, mk, mv, mdo, mdq, p, s)
+                 : launch_bwd_t<64, false>(mq, mk, mv, mdo, mdq, p, s);
+  return split ? launch_bwd_t<128, true>(mq, mk, mv, mdo, mdq, p, s)
+               : launch_bwd_t<128, false>(mq, mk, mv, mdo, mdq, p, s);
 }
 
 cudaError_t launch_dq_convert(int d, const float* dq_accum, float scale, uint16_t* dq,

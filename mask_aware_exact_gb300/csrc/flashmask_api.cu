@@ -447,11 +447,10 @@ fm_status flashmask_bwd_main(const void* q, const void* k, const void* v, const 
   const long long rows_pad = heads * padded(N);
   char* w = static_cast<char*>(ws);
   float* dq_accum = reinterpret_cast<float*>(w + L.dq_accum);
-  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!make_map3(&mq, q, heads, N, d, 2) || !make_map3(&mk, k, heads, N, d, 2) ||
       !make_map3(&mv, v, heads, N, d, 2) || !make_map3(&mdo, dout, heads, N, d, 2) ||
-      !make_map_f32(&mdq, dq_accum, rows_pad, d) || !make_map3(&mdk, dk, heads, N, d, 2) ||
-      !make_map3(&mdv, dv, heads, N, d, 2))
+      !make_map_f32(&mdq, dq_accum, rows_pad, d))
     return FM_ERR_CUDA;
   const fm::ClassifyTables t = tables(L, ws);
   fm::BwdParams p;
@@ -473,10 +472,14 @@ fm_status flashmask_bwd_main(const void* q, const void* k, const void* v, const 
   p.split_e = p.Tc >= split_min_blocks() ? fm::split_blocks(p.Tc) : 0;
   p.kv_part = reinterpret_cast<float*>(w + L.kv_part);
   p.kv_sync = reinterpret_cast<int32_t*>(w + L.kv_sync);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.num_sms = sm_count();
+  if (p.num_sms <= 0) return FM_ERR_CUDA;
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
   p.status = reinterpret_cast<int32_t*>(w + L.status);
-  return fm::launch_bwd(d, mq, mk, mv, mdo, mdq, mdk, mdv, p, static_cast<cudaStream_t>(stream)) ==
+  return fm::launch_bwd(d, mq, mk, mv, mdo, mdq, p, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? FM_OK
              : FM_ERR_CUDA;

@@ -106,6 +106,9 @@ struct BwdParams {
   int32_t* kv_sync;    // [B,H,E,kSyncWords]: arrivals, then one ready flag per slot
   uint16_t* dk;
   uint16_t* dv;
+  const uint16_t* k;  // K and V, for the L2 prefetch of a later CTA's blocks
+  const uint16_t* v;
+  int num_sms;        // CTAs resident at once (one per SM)
   int32_t* status;
 };
 
@@ -122,8 +125,7 @@ cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const
                            int Npad, const int32_t* zero_tag_word, int32_t zero_tag,
                            int32_t* kv_sync, int split_e, cudaStream_t s);
 cudaError_t launch_bwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const CUtensorMap& mdo, const CUtensorMap& mdq, const CUtensorMap& mdk,
-                       const CUtensorMap& mdv, const BwdParams& p,
+                       const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p,
                        cudaStream_t s);
 cudaError_t launch_dq_convert(int d, const float* dq_accum, float scale, uint16_t* dq,
                               long long heads, int N, int Npad, cudaStream_t s);
