@@ -58,7 +58,7 @@ E2E_CHUNK_HEADS = 2
 # scaled by 4 to H = 32: every head is an independent unit of identical work,
 # so traffic grows in proportion to the heads.
 NCU_TRAFFIC = {
-    "bwd_main@b37e88d68a06@document_b1h32n32768d128": 4 * (405.965824e6 + 220.268800e6),
+    "bwd_main@cfd872d4df87@document_b1h32n32768d128": 4 * (410.560512e6 + 221.885184e6),
     "fwd@196fd6b00911@document_b1h32n32768d128": 4 * (204.520704e6 + 164.038912e6),
 }
 
