@@ -291,9 +291,9 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
   const fm_status ws_st = check_ws(ws, ws_bytes, L);
   if (ws_st != FM_OK) return ws_st;
   const long long heads = static_cast<long long>(B) * H;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map3(&mq, q, heads, N, d, 2) || !make_map3(&mk, k, heads, N, d, 2) ||
-      !make_map3(&mv, v, heads, N, d, 2))
+      !make_map3(&mv, v, heads, N, d, 2) || !make_map3(&mo, o, heads, N, d, 2))
     return FM_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const fm::ClassifyTables t = tables(L, ws);
@@ -325,7 +325,7 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
                   ? reinterpret_cast<float*>(static_cast<char*>(ws) + Lb.dq_accum)
                   : nullptr;
   p.dq_tag = dq_zero_tag(B, H, mask->Hm, N, d);
-  return fm::launch_fwd(d, mq, mk, mv, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+  return fm::launch_fwd(d, mq, mk, mv, mo, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
 size_t flashmask_fwd_fp8_workspace_bytes(int B, int H, int Hm, int N) {
@@ -370,9 +370,10 @@ fm_status flashmask_fwd_fp8(const void* q, const void* k, const void* v, const f
   f.vscale = reinterpret_cast<float*>(w + F.vscale);
   f.vamax = reinterpret_cast<unsigned int*>(w + F.vamax);
   const int BH = B * H;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map3(&mq, f.q8, BH, N, 128, 1) || !make_map3(&mk, f.k8, BH, N, 128, 1) ||
-      !make_map_u8(&mv, f.vt8, static_cast<long long>(BH) * 128, padded(N)))
+      !make_map_u8(&mv, f.vt8, static_cast<long long>(BH) * 128, padded(N)) ||
+      !make_map3(&mo, o, BH, N, 128, 2))
     return FM_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const fm::ClassifyTables t = tables(F.base, ws);
@@ -406,7 +407,7 @@ fm_status flashmask_fwd_fp8(const void* q, const void* k, const void* v, const f
   // clears the tag, so a later backward preprocess zeroes it again
   p.dq_zero = nullptr;
   p.dq_tag = 0;
-  return fm::launch_fwd_fp8(mq, mk, mv, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+  return fm::launch_fwd_fp8(mq, mk, mv, mo, p, s) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
 fm_status flashmask_bwd_preprocess(const void* o, const float* lse, const void* dout, int B, int H,

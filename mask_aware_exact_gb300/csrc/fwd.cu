@@ -83,7 +83,10 @@ struct FwdLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;             // kKSlots x kTileBytes
   static constexpr int kV = kK + kKSlots * kTileBytes;   // kVSlots x kTileBytes
-  static constexpr int kRed = kV + kVSlots * kTileBytes;  // fp32 [m, l][2 groups][128]
+  // bf16 O staging for the TMA stores: 128 rows x D, as 128-byte swizzled
+  // 64-column halves of 16 KB
+  static constexpr int kOStage = kV + kVSlots * kTileBytes;
+  static constexpr int kRed = kOStage + kTile * D * 2;  // fp32 [m, l][2 groups][128]
   static constexpr int kBar = kRed + 2 * 2 * kTile * 4;
   // q_full, k_full[2], v_full[2], s_full[2], p_full[2], pv_done[2],
   // sched_full[2], sched_empty[2], o_free. K slot, V slot and S region of step
@@ -99,6 +102,12 @@ struct FwdLayout {
   static constexpr int kZeroBytes = kFp8 ? 0 : 16384;
   static constexpr int kBytes = kZero + kZeroBytes;
 };
+
+static_assert(FwdLayout<128, false>::kOStage % 1024 == 0 &&
+                  FwdLayout<64, false>::kOStage % 1024 == 0 &&
+                  FwdLayout<128, true>::kOStage % 1024 == 0,
+              "the 128-byte swizzle of the O staging buffer needs 1024-byte alignment");
+static_assert(FwdLayout<128, false>::kBytes <= 227 * 1024, "shared memory per CTA");
 
 struct FwdBars {
   uint32_t base;
@@ -147,11 +156,25 @@ __device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, float f) {
   }
 }
 
-// Writes n = 32 TMEM columns of this lane's row as bf16 after merging two
-// accumulators, f0 * A + f1 * B (the TMEM loads run on every lane of the warp;
-// only lanes with `store` write).
-__device__ __forceinline__ void tmem_merge_to_bf16(uint32_t ta, uint32_t tb, bool live, float f0,
-                                                   float f1, uint16_t* dst, bool store) {
+// 3-D tiled store of one box from shared memory (x, y, z = column, row within
+// the head, head), in the current bulk async-group; rows outside the tensor
+// map (beyond the head's length) are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+
+// Merges 32 TMEM columns of this lane's row from two accumulators, f0 * A +
+// f1 * B (the TMEM loads run on every lane of the warp), and writes them as
+// bf16 to 64 bytes of the row's 128-byte swizzled staging row, 16-byte units
+// [unit0, unit0 + 4).
+__device__ __forceinline__ void tmem_merge_to_stage(uint32_t ta, uint32_t tb, bool live, float f0,
+                                                    float f1, uint32_t stage_half, int row,
+                                                    int unit0) {
   uint32_t a[32], b[32];
   if (live) {
     tmem_ld32(ta, a);
@@ -160,11 +183,15 @@ __device__ __forceinline__ void tmem_merge_to_bf16(uint32_t ta, uint32_t tb, boo
 #pragma unroll
     for (int i = 0; i < 32; ++i) a[i] = b[i] = 0u;
   }
-  if (!store) return;  // after the (warp-collective) TMEM loads
+  uint32_t w16[16];
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    a[i] = __float_as_uint(__uint_as_float(a[i]) * f0 + __uint_as_float(b[i]) * f1);
-  store_row32_bf16(dst, a, 1.f);
+  for (int i = 0; i < 16; ++i)
+    w16[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * f0 + __uint_as_float(b[2 * i]) * f1,
+                         __uint_as_float(a[2 * i + 1]) * f0 + __uint_as_float(b[2 * i + 1]) * f1);
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    st_shared_v4(stage_half + sw128_offset(row, unit0 + u), w16[4 * u], w16[4 * u + 1],
+                 w16[4 * u + 2], w16[4 * u + 3]);
 }
 
 // kShortLast: N is not a multiple of 128. kFp8 (d = 128 only): e4m3 Q, K and
@@ -185,7 +212,8 @@ __device__ __forceinline__ void tmem_merge_to_bf16(uint32_t ta, uint32_t tb, boo
 template <int D, bool kShortLast, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-               const __grid_constant__ CUtensorMap mv, const FwdParams p) {
+               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mo,
+               const FwdParams p) {
   using L = FwdLayout<D, kFp8>;
   static_assert(!kFp8 || D == 128, "the FP8 forward is for d = 128");
   constexpr int kOCols = D / 2;  // O columns per softmax warpgroup
@@ -198,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK),
-                 sV = smem_u32(smem + L::kV);
+                 sV = smem_u32(smem + L::kV), sO = smem_u32(smem + L::kOStage);
   float* red = reinterpret_cast<float*>(smem + L::kRed);
   // [0, 2): the item ring; [2, 4): the item as the softmax warps share it
   volatile int* sched = reinterpret_cast<volatile int*>(smem + L::kSched);
@@ -653,6 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulators, O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1)
       red[w * kTile + row] = m;
       red[(2 + w) * kTile + row] = l;
+      // the O staging buffer is free once the previous item's stores have
+      // read it (long done: a whole item ago)
+      if (tid == 0) bulk_wait_read_all();
       softmax_bar();
       const float m_o = red[(w ^ 1) * kTile + row], l_o = red[(2 + (w ^ 1)) * kTile + row];
       const float m_all = fmaxf(m, m_o);
@@ -664,14 +695,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // FP8: O accumulated (kFp8PScale P) (V / scale_V)
       const float inv = has ? (kFp8 ? p.vscale[bh] * (1.f / kFp8PScale) : 1.f) / ltot : 0.f;
       const float f0 = (w == 0 ? f_self : f_oth) * inv, f1 = (w == 0 ? f_oth : f_self) * inv;
-      // rows >= N of a short last query block do not exist: nothing is stored
+      // rows >= N of a short last query block do not exist: no LSE for them
+      // (their O rows lie outside the tensor map and are not stored)
       const bool row_exists = !kShortLast || r * kTile + row < p.N;
-      uint16_t* orow = p.o + static_cast<size_t>(it.q_row0 + row) * D + w * kOCols;
+      // this warpgroup's columns [w D/2, w D/2 + D/2) of the row go to the
+      // staging buffer: half w for d = 128, units [4w, 4w + 4) of the single
+      // half for d = 64; one thread then stores the tile with TMA, so the
+      // softmax warps issue no global stores of O
 #pragma unroll
       for (int ch = 0; ch < kOCols / 32; ++ch)
-        tmem_merge_to_bf16(tmem + lane_base + col_o(0) + w * kOCols + 32 * ch,
-                           tmem + lane_base + col_o(1) + w * kOCols + 32 * ch, live, f0, f1,
-                           orow + 32 * ch, row_exists);
+        tmem_merge_to_stage(tmem + lane_base + col_o(0) + w * kOCols + 32 * ch,
+                            tmem + lane_base + col_o(1) + w * kOCols + 32 * ch, live, f0, f1,
+                            sO + (D == 128 ? w * 16384 : 0), row, D == 128 ? 4 * ch : 4 * w);
       if (ntiles > 0) {
         // O_0 and O_1 have been read (the loads above completed): the next
         // item's first products may overwrite them
@@ -679,6 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar.o_free());
       }
+      fence_proxy_async_smem();  // the staged rows are read by the TMA engine
       if (w == 0 && row_exists) {
         const float m_fin = (m_all == -INFINITY) ? 0.f : m_all;
         p.lse[it.q_row0 + row] =
@@ -686,9 +722,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       J += ntiles;
       // every warp has read the exchange buffer before the next item's
-      // epilogue writes it
+      // epilogue writes it, and has staged its O rows
       softmax_bar();
+      if (tid == 0) {
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          tma_store_3d(&mo, sO + hf * 16384, 64 * hf, r * kTile, bh);
+        bulk_commit_group();
+      }
     }
+    if (tid == 0) bulk_wait_read_all();  // the last O stores, before the CTA exits
   }
 
   tc_fence_before();
@@ -701,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool kShortLast, bool kFp8 = false>
 cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const FwdParams& p, cudaStream_t s) {
+                         const CUtensorMap& mo, const FwdParams& p, cudaStream_t s) {
   using L = FwdLayout<D, kFp8>;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kShortLast, kFp8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
@@ -712,26 +755,27 @@ cudaError_t launch_fwd_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   const unsigned grid = static_cast<unsigned>(items < p.num_sms ? items : p.num_sms);
   e = cudaMemsetAsync(p.sched, 0, sizeof(int32_t), s);
   if (e != cudaSuccess) return e;
-  fwd_kernel<D, kShortLast, kFp8><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, p);
+  fwd_kernel<D, kShortLast, kFp8><<<grid, kThreads, L::kBytes, s>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const FwdParams& p, cudaStream_t s) {
+                       const CUtensorMap& mo, const FwdParams& p, cudaStream_t s) {
   const bool short_last = p.N % kTile != 0;
   if (d == 64)
-    return short_last ? launch_fwd_t<64, true>(mq, mk, mv, p, s)
-                      : launch_fwd_t<64, false>(mq, mk, mv, p, s);
-  return short_last ? launch_fwd_t<128, true>(mq, mk, mv, p, s)
-                    : launch_fwd_t<128, false>(mq, mk, mv, p, s);
+    return short_last ? launch_fwd_t<64, true>(mq, mk, mv, mo, p, s)
+                      : launch_fwd_t<64, false>(mq, mk, mv, mo, p, s);
+  return short_last ? launch_fwd_t<128, true>(mq, mk, mv, mo, p, s)
+                    : launch_fwd_t<128, false>(mq, mk, mv, mo, p, s);
 }
 
 cudaError_t launch_fwd_fp8(const CUtensorMap& mq8, const CUtensorMap& mk8,
-                           const CUtensorMap& mvt8, const FwdParams& p, cudaStream_t s) {
-  return p.N % kTile != 0 ? launch_fwd_t<128, true, true>(mq8, mk8, mvt8, p, s)
-                          : launch_fwd_t<128, false, true>(mq8, mk8, mvt8, p, s);
+                           const CUtensorMap& mvt8, const CUtensorMap& mo, const FwdParams& p,
+                           cudaStream_t s) {
+  return p.N % kTile != 0 ? launch_fwd_t<128, true, true>(mq8, mk8, mvt8, mo, p, s)
+                          : launch_fwd_t<128, false, true>(mq8, mk8, mvt8, mo, p, s);
 }
 
 }  // namespace fm

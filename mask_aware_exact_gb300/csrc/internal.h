@@ -115,9 +115,10 @@ struct BwdParams {
 cudaError_t launch_classify(const MaskDev& m, int B, int N, const ClassifyTables& t,
                             cudaStream_t s);
 cudaError_t launch_fwd(int d, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const FwdParams& p, cudaStream_t s);
+                       const CUtensorMap& mo, const FwdParams& p, cudaStream_t s);
 cudaError_t launch_fwd_fp8(const CUtensorMap& mq8, const CUtensorMap& mk8,
-                           const CUtensorMap& mvt8, const FwdParams& p, cudaStream_t s);
+                           const CUtensorMap& mvt8, const CUtensorMap& mo, const FwdParams& p,
+                           cudaStream_t s);
 cudaError_t launch_quant_fp8(const uint16_t* q, const uint16_t* k, const uint16_t* v, int BH,
                              int N, const Fp8Operands& f, cudaStream_t s);
 cudaError_t launch_bwd_pre(int d, const uint16_t* o, const uint16_t* dout, const float* lse,
