@@ -94,8 +94,10 @@ struct FwdLayout {
   // also frees V slot J % 2.
   static_assert(kKSlots == kSRegions && kVSlots == kSRegions, "slots follow the S regions");
   static constexpr int kNumBars = 1 + kKSlots + kVSlots + 3 * kSRegions + 5;
-  static constexpr int kSched = kBar + kNumBars * 8;  // int[4]
-  static constexpr int kTmemSlot = kSched + 16;
+  // int[8] x 4: the item ring (two entries), then the item as softmax warp 0
+  // shares it (two entries)
+  static constexpr int kSched = (kBar + kNumBars * 8 + 31) / 32 * 32;
+  static constexpr int kTmemSlot = kSched + 128;
   // 16 KB of zeros, the source of the bulk copies that clear the dQ
   // accumulator rows of each query block (bf16 forward only)
   static constexpr int kZero = kTmemSlot + 16;
@@ -108,6 +110,10 @@ static_assert(FwdLayout<128, false>::kOStage % 1024 == 0 &&
                   FwdLayout<128, true>::kOStage % 1024 == 0,
               "the 128-byte swizzle of the O staging buffer needs 1024-byte alignment");
 static_assert(FwdLayout<128, false>::kBytes <= 227 * 1024, "shared memory per CTA");
+static_assert(FwdLayout<128, false>::kSched % 32 == 0 && FwdLayout<64, false>::kSched % 32 == 0 &&
+                  FwdLayout<128, true>::kSched % 32 == 0,
+              "the item ring is read and written with 16-byte shared-memory accesses");
+static_assert(FwdLayout<128, false>::kZero % 16 == 0, "bulk copies read 16-byte aligned sources");
 
 struct FwdBars {
   uint32_t base;
@@ -134,6 +140,17 @@ struct FwdBars {
 // V producer and softmax warp 0 (which shares it with the other seven).
 constexpr int kSchedReaders = 4;
 
+
+__device__ __forceinline__ void ld_shared_v4i(uint32_t addr, int& a, int& b, int& c, int& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void st_shared_v4i(uint32_t addr, int a, int b, int c, int d) {
+  st_shared_v4(addr, static_cast<uint32_t>(a), static_cast<uint32_t>(b), static_cast<uint32_t>(c),
+               static_cast<uint32_t>(d));
+}
 
 // The 256 softmax threads (both warpgroups).
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -228,8 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + L::kQ), sK = smem_u32(smem + L::kK),
                  sV = smem_u32(smem + L::kV), sO = smem_u32(smem + L::kOStage);
   float* red = reinterpret_cast<float*>(smem + L::kRed);
-  // [0, 2): the item ring; [2, 4): the item as the softmax warps share it
-  volatile int* sched = reinterpret_cast<volatile int*>(smem + L::kSched);
+  // int[8] entries: [0, 2) the item ring, [2, 4) the item as softmax warp 0
+  // shares it with the other seven
+  const uint32_t ring = smem_u32(smem + L::kSched), share = ring + 64;
   const FwdBars bar{smem_u32(smem + L::kBar)};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
@@ -268,35 +286,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Work item n: head-major, longest query blocks of each head first, so the
   // CTAs working at the same time share one head's K and V in L2.
+  // The scheduler looks up everything an item needs once and publishes it:
+  // {n, r (query block), ntiles, first list entry, bh (head), bm (mask
+  // head), -, -}, n = -1 when no item is left. The other roles then start an
+  // item without global loads or integer divisions on their paths.
   struct Item {
-    int bh, bm, r, ntiles, head_row0, q_row0;
+    int n, bh, bm, r, ntiles, first, head_row0, q_row0;
     const int32_t* list;
   };
-  auto decode = [&](int n) -> Item {
+  auto make_item = [&](const int (&v)[8]) -> Item {
     Item it;
-    it.bh = n / p.Tr;
-    const int rank = n % p.Tr;
-    const int b = it.bh / p.H, h = it.bh % p.H;
-    it.bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
-    it.r = p.row_order[static_cast<size_t>(it.bm) * p.Tr + rank];
-    it.ntiles = p.row_count[static_cast<size_t>(it.bm) * p.Tr + it.r];
+    it.n = v[0];
+    it.r = v[1];
+    it.ntiles = v[2];
+    it.first = v[3];
+    it.bh = v[4];
+    it.bm = v[5];
     it.list = p.row_list + (static_cast<size_t>(it.bm) * p.Tr + it.r) * p.Tc;
     it.head_row0 = it.bh * p.N;               // first row of this head in [B*H*N, d]
     it.q_row0 = it.head_row0 + it.r * kTile;  // first query row of the block
     return it;
   };
-  // The k-th item of this CTA (k = 0, 1, ...) from the ring, or -1 when no
-  // item is left or the wait gave up (then `ok` is false).
-  auto read_item = [&](int k, bool& ok) -> int {
+  // The k-th item of this CTA (k = 0, 1, ...) from the ring into v (n = -1
+  // when no item is left or the wait gave up; then `ok` is false).
+  auto read_item = [&](int k, int (&v)[8], bool& ok) {
     const int s = k & 1;
+    v[0] = -1;
+    v[1] = v[2] = v[3] = v[4] = v[5] = v[6] = v[7] = 0;
     if (!mbar_wait(bar.sched_full(s), (k >> 1) & 1, p.status)) {
       record_failure(p.status, kStatusTimeout, kSiteFwdSched);
       ok = false;
-      return -1;
+      return;
     }
-    const int n = sched[s];
+    ld_shared_v4i(ring + 32 * s, v[0], v[1], v[2], v[3]);
+    ld_shared_v4i(ring + 32 * s + 16, v[4], v[5], v[6], v[7]);
     mbar_arrive(bar.sched_empty(s));
-    return n;
+  };
+  auto take_item = [&](int k, bool& ok) -> Item {
+    int v[8];
+    read_item(k, v, ok);
+    return make_item(v);
   };
 
   if (warp == 8) {
@@ -304,9 +333,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mk);
-      auto claim = [&]() -> int {
+      // claims an item and looks up its ring entry
+      auto claim = [&](int (&v)[8]) {
+        v[0] = -1;
+        v[1] = v[2] = v[3] = v[4] = v[5] = v[6] = v[7] = 0;
         const int n = atomicAdd(p.sched, 1);
-        return n < n_items ? n : -1;
+        if (n >= n_items) return;
+        const int bh = n / p.Tr, rank = n % p.Tr;
+        const int b = bh / p.H, h = bh % p.H;
+        const int bm = b * p.mask.Hm + h / (p.H / p.mask.Hm);
+        const size_t mr = static_cast<size_t>(bm) * p.Tr;
+        const int r = p.row_order[mr + rank];
+        const int nt = p.row_count[mr + r];
+        v[0] = n;
+        v[1] = r;
+        v[2] = nt;
+        v[3] = nt > 0 ? p.row_list[(mr + r) * p.Tc] : 0;
+        v[4] = bh;
+        v[5] = bm;
+      };
+      auto publish = [&](int s, const int (&v)[8]) {
+        st_shared_v4i(ring + 32 * s, v[0], v[1], v[2], v[3]);
+        st_shared_v4i(ring + 32 * s + 16, v[4], v[5], v[6], v[7]);
+        mbar_arrive(bar.sched_full(s));
       };
       // K of step J into slot J % 2 once S_{J-2} has completed; kb is the
       // key block, bh the head (3-D map: rows past the head's end read zeros)
@@ -323,13 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       bar.k_full(slot));
         return true;
       };
-      int cur = claim();
-      sched[0] = cur;
-      mbar_arrive(bar.sched_full(0));
+      int cur[8];
+      claim(cur);
+      publish(0, cur);
       bool ok = true;
       int J = 0, J_last = -1;  // running step; last step of the previous item with tiles
-      for (int k = 0; ok && cur >= 0; ++k) {
-        const Item it = decode(cur);
+      for (int k = 0; ok && cur[0] >= 0; ++k) {
+        const Item it = make_item(cur);
         if (it.ntiles > 0) {
           // the Q buffer is free once the last S of the previous item is done
           if (J_last >= 0 && !mbar_wait(bar.s_full(J_last % kSRegions),
@@ -341,8 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar.q_full(), L::kTileBytes);
           for (int ch = 0; ch < L::kChunks; ++ch)
             tma_load_3d(sQ + ch * L::kChunk, &mq, ch * 64, it.r * kTile, it.bh, bar.q_full());
-          for (int j = 0; ok && j < it.ntiles; ++j, ++J)
-            ok = load_k(J, it.list[j] >> 2, it.bh);
+          int e_next = it.first;  // list entries read one step ahead
+          for (int j = 0; ok && j < it.ntiles; ++j, ++J) {
+            const int e = e_next;
+            if (j + 1 < it.ntiles) e_next = it.list[j + 1];
+            ok = load_k(J, e >> 2, it.bh);
+          }
           J_last = J - 1;
         }
         if constexpr (!kFp8) {
@@ -362,16 +415,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // claim the next item once this one's loads are issued; its ring
         // entry was last used by item k - 1, which every reader has taken
-        const int nxt = claim();
+        int nxt[8];
+        claim(nxt);
         const int s = (k + 1) & 1;
         if (k >= 1 && !mbar_wait(bar.sched_empty(s), ((k - 1) >> 1) & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteFwdSched);
           ok = false;
           break;
         }
-        sched[s] = nxt;
-        mbar_arrive(bar.sched_full(s));
-        cur = nxt;
+        publish(s, nxt);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
       }
       if constexpr (!kFp8) bulk_wait_all();  // the zeroing copies, before the CTA exits
     }
@@ -382,11 +436,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int J = 0;
       for (int k = 0; ok; ++k) {
-        const int n = read_item(k, ok);
-        if (n < 0) break;
-        const Item it = decode(n);
+        const Item it = take_item(k, ok);
+        if (it.n < 0) break;
+        int e_next = it.first;  // list entries read one step ahead
         for (int j = 0; ok && j < it.ntiles; ++j, ++J) {
           const int slot = J % kVSlots;
+          const int kb = e_next >> 2;
+          if (j + 1 < it.ntiles) e_next = it.list[j + 1];
           if (J >= kVSlots &&
               !mbar_wait(bar.pv_done(slot), ((J / kVSlots) - 1) & 1, p.status)) {
             record_failure(p.status, kStatusTimeout, kSiteFwdVEmpty);
@@ -396,12 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar.v_full(slot), L::kTileBytes);
           if constexpr (kFp8) {
             // V^T tile: the head's 128 rows of d, the block's 128 keys
-            tma_load_2d(sV + slot * L::kTileBytes, &mv, (it.list[j] >> 2) * kTile, it.bh * 128,
+            tma_load_2d(sV + slot * L::kTileBytes, &mv, kb * kTile, it.bh * 128,
                         bar.v_full(slot));
           } else {
             for (int ch = 0; ch < L::kChunks; ++ch)
-              tma_load_3d(sV + slot * L::kTileBytes + ch * L::kChunk, &mv, ch * 64,
-                          (it.list[j] >> 2) * kTile, it.bh, bar.v_full(slot));
+              tma_load_3d(sV + slot * L::kTileBytes + ch * L::kChunk, &mv, ch * 64, kb * kTile,
+                          it.bh, bar.v_full(slot));
           }
         }
       }
@@ -420,9 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int J = 0, ti = 0;  // running step; items with tiles so far
       for (int k = 0; ok; ++k) {
-        const int n = read_item(k, ok);
-        if (n < 0) break;
-        const int ntiles = decode(n).ntiles;
+        const Item it = take_item(k, ok);
+        if (it.n < 0) break;
+        const int ntiles = it.ntiles;
         if (ntiles == 0) continue;
         if (!mbar_wait(bar.q_full(), ti & 1, p.status)) {
           record_failure(p.status, kStatusTimeout, kSiteFwdQ);
@@ -475,9 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int J = 0, ti = 0;
       for (int k = 0; ok; ++k) {
-        const int n = read_item(k, ok);
-        if (n < 0) break;
-        const int ntiles = decode(n).ntiles;
+        const Item it = take_item(k, ok);
+        if (it.n < 0) break;
+        const int ntiles = it.ntiles;
         if (ntiles == 0) continue;
         for (int j = 0; j < ntiles; ++j, ++J) {
           const int g = J % kSRegions, vs = J % kVSlots;
@@ -531,19 +587,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // memory, so that the eight warps agree on it even after a failure
       if (warp == 0 && lane == 0) {
         bool okr = true;
-        sched[2 + (k & 1)] = read_item(k, okr);
+        int v[8];
+        read_item(k, v, okr);
+        st_shared_v4i(share + 32 * (k & 1), v[0], v[1], v[2], v[3]);
+        st_shared_v4i(share + 32 * (k & 1) + 16, v[4], v[5], v[6], v[7]);
       }
       softmax_bar();
-      const int n = sched[2 + (k & 1)];
-      if (n < 0) break;
-      const Item it = decode(n);
+      int v[8];
+      ld_shared_v4i(share + 32 * (k & 1), v[0], v[1], v[2], v[3]);
+      ld_shared_v4i(share + 32 * (k & 1) + 16, v[4], v[5], v[6], v[7]);
+      if (v[0] < 0) break;
+      const Item it = make_item(v);
       const int ntiles = it.ntiles, r = it.r, bh = it.bh, bm = it.bm;
       // FP8: the true score is S times scale_Q(query block) * scale_K(key
       // block); the product folds into each tile's exponent scale c
       const float c_row = kFp8 ? p.scale_log2 * p.qscale[static_cast<size_t>(bh) * p.Tr + r]
                                : p.scale_log2;
       float m = -INFINITY, l = 0.f;
-      int next_entry = ntiles > 0 ? it.list[0] : 0;  // read one step ahead
+      int next_entry = it.first;  // list entries read one step ahead
       for (int j = 0; j < ntiles; ++j) {
         const int Jj = J + j;
         const int entry = next_entry;
