@@ -59,7 +59,7 @@ E2E_CHUNK_HEADS = 2
 # so traffic grows in proportion to the heads.
 NCU_TRAFFIC = {
     "bwd_main@cfd872d4df87@document_b1h32n32768d128": 4 * (410.560512e6 + 221.885184e6),
-    "fwd@196fd6b00911@document_b1h32n32768d128": 4 * (204.520704e6 + 164.038912e6),
+    "fwd@7a7ce797666a@document_b1h32n32768d128": 4 * (205.098752e6 + 165.101312e6),
 }
 
 
@@ -330,17 +330,23 @@ def run_native(args):
 
     for _ in range(args.warmup):
         e2e_step()
+    # three timed groups of K2 steps; the median group is reported (the host
+    # side of each call, the copies' path through host memory and the other
+    # work on the host make single groups vary by tens of percent)
     K2 = max(3, K // 2)
-    R.barrier()
-    torch.cuda.synchronize()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(K2):
-        e2e_step()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    R.barrier()
-    e2e_s = a0.elapsed_time(a1) / 1e3
+    groups = []
+    for _ in range(3):
+        R.barrier()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(K2):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        R.barrier()
+        groups.append(a0.elapsed_time(a1) / 1e3)
+    e2e_s = sorted(groups)[1]
     e2e_agg = R.aggregate_throughput(fl["total"] * K2, e2e_s, dev)
     del hws
 
@@ -449,7 +455,10 @@ def run_native(args):
             "e2e": {"value": round(e2e_agg["throughput"] / 1e12, 2), "unit": UNIT,
                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "api": "flashmask_fwd_bwd_host", "chunk_heads": chunk,
-                    "ms_per_step": round(e2e_agg["max_elapsed_s"] / K2 * 1e3, 4)},
+                    "ms_per_step": round(e2e_agg["max_elapsed_s"] / K2 * 1e3, 4),
+                    "steps_per_group": K2,
+                    "group_ms_per_step": [round(g / K2 * 1e3, 4) for g in groups],
+                    "reported": "median of three timed groups"},
             "gpu_launches": 7 * K,
             "clocks": clk,
         }
