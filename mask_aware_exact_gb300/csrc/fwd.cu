@@ -33,7 +33,8 @@
 //              (log2 domain), and writes its P slice into TMEM. O_w is
 //              rescaled only when that max grows by more than 2^8 (lazy
 //              rescaling: exact after the final division). Epilogue: merge of
-//              the two halves, O and LSE.
+//              the two halves, O (staged, stored by TMA) and LSE, run one
+//              item late, inside the next item's first step.
 //   warp 8     work scheduler and TMA producer of Q (once per item) and K
 //              blocks (two-slot ring).
 //   warp 9     S issuer (one thread): S_j once K_j has landed and the P V
@@ -582,6 +583,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the CTA can still reach its exit; `ok` is kept uniform across the warp.
     bool ok = true;
     int J = 0;  // running step
+    // The epilogue of an item (query block r of head bh whose last step was
+    // jl; has_tiles = 0 for an item no key sees): the two halves' states are
+    // merged, O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1), staged as bf16
+    // and stored by TMA, and LSE written. It runs one item late, inside the
+    // next item's first step once that step's P has been written, so that the
+    // last P V products of the item have completed by then and the next
+    // item's first S and softmax step overlap them instead of waiting.
+    auto finish = [&](float m_, float l_, int r_, int bh_, int has_tiles, int jl) {
+      if (ok && has_tiles) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(jl % kSRegions),
+                                               (jl / kSRegions) & 1, p.status));
+        if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdO);
+        tc_fence_after();
+      }
+      // each warpgroup publishes its row maximum and sum
+      red[w * kTile + row] = m_;
+      red[(2 + w) * kTile + row] = l_;
+      // the O staging buffer is free once the previous item's stores have
+      // read it (long done: a whole item ago)
+      if (tid == 0) bulk_wait_read_all();
+      softmax_bar();
+      const float m_o = red[(w ^ 1) * kTile + row], l_o = red[(2 + (w ^ 1)) * kTile + row];
+      const float m_all = fmaxf(m_, m_o);
+      const float f_self = (m_ == -INFINITY) ? 0.f : ex2(m_ - m_all);
+      const float f_oth = (m_o == -INFINITY) ? 0.f : ex2(m_o - m_all);
+      const float ltot = l_ * f_self + l_o * f_oth;
+      const bool live = ok && has_tiles;
+      const bool has = live && ltot > 0.f;
+      // FP8: O accumulated (kFp8PScale P) (V / scale_V)
+      const float inv = has ? (kFp8 ? p.vscale[bh_] * (1.f / kFp8PScale) : 1.f) / ltot : 0.f;
+      const float f0 = (w == 0 ? f_self : f_oth) * inv, f1 = (w == 0 ? f_oth : f_self) * inv;
+      // rows >= N of a short last query block do not exist: no LSE for them
+      // (their O rows lie outside the tensor map and are not stored)
+      const bool row_exists = !kShortLast || r_ * kTile + row < p.N;
+      // this warpgroup's columns [w D/2, w D/2 + D/2) of the row go to the
+      // staging buffer: half w for d = 128, units [4w, 4w + 4) of the single
+      // half for d = 64; one thread then stores the tile with TMA, so the
+      // softmax warps issue no global stores of O
+#pragma unroll
+      for (int ch = 0; ch < kOCols / 32; ++ch)
+        tmem_merge_to_stage(tmem + lane_base + col_o(0) + w * kOCols + 32 * ch,
+                            tmem + lane_base + col_o(1) + w * kOCols + 32 * ch, live, f0, f1,
+                            sO + (D == 128 ? w * 16384 : 0), row, D == 128 ? 4 * ch : 4 * w);
+      if (has_tiles) {
+        // O_0 and O_1 have been read (the loads above completed): the next
+        // item's first products may overwrite them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.o_free());
+      }
+      fence_proxy_async_smem();  // the staged rows are read by the TMA engine
+      if (w == 0 && row_exists) {
+        const float m_fin = (m_all == -INFINITY) ? 0.f : m_all;
+        p.lse[static_cast<size_t>(bh_) * p.N + r_ * kTile + row] =
+            has ? (m_fin + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
+      }
+      // every warp has read the exchange buffer before the next epilogue
+      // writes it, and has staged its O rows
+      softmax_bar();
+      if (tid == 0) {
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          tma_store_3d(&mo, sO + hf * 16384, 64 * hf, r_ * kTile, bh_);
+        bulk_commit_group();
+      }
+    };
+    bool pend = false;  // an item whose epilogue is still to run
+    float pend_m = 0.f, pend_l = 0.f;
+    int pend_r = 0, pend_bh = 0, pend_jl = 0;
     for (int k = 0;; ++k) {
       // warp 0 takes the item from the ring and shares it through shared
       // memory, so that the eight warps agree on it even after a failure
@@ -728,70 +798,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar.p_full(g));
+        if (j == 0 && pend) {
+          finish(pend_m, pend_l, pend_r, pend_bh, 1, pend_jl);
+          pend = false;
+        }
       }
-      // ---------------------------------------------------------- epilogue of the item
-      if (ok && ntiles > 0) {
-        const int jl = J + ntiles - 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar.pv_done(jl % kSRegions),
-                                               (jl / kSRegions) & 1, p.status));
-        if (!ok && lane == 0) record_failure(p.status, kStatusTimeout, kSiteFwdO);
-        tc_fence_after();
-      }
-      // merge the two halves' states: each warpgroup publishes its row maximum
-      // and sum, then writes its half of the output columns from both
-      // accumulators, O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1)
-      red[w * kTile + row] = m;
-      red[(2 + w) * kTile + row] = l;
-      // the O staging buffer is free once the previous item's stores have
-      // read it (long done: a whole item ago)
-      if (tid == 0) bulk_wait_read_all();
-      softmax_bar();
-      const float m_o = red[(w ^ 1) * kTile + row], l_o = red[(2 + (w ^ 1)) * kTile + row];
-      const float m_all = fmaxf(m, m_o);
-      const float f_self = (m == -INFINITY) ? 0.f : ex2(m - m_all);
-      const float f_oth = (m_o == -INFINITY) ? 0.f : ex2(m_o - m_all);
-      const float ltot = l * f_self + l_o * f_oth;
-      const bool live = ok && ntiles > 0;
-      const bool has = live && ltot > 0.f;
-      // FP8: O accumulated (kFp8PScale P) (V / scale_V)
-      const float inv = has ? (kFp8 ? p.vscale[bh] * (1.f / kFp8PScale) : 1.f) / ltot : 0.f;
-      const float f0 = (w == 0 ? f_self : f_oth) * inv, f1 = (w == 0 ? f_oth : f_self) * inv;
-      // rows >= N of a short last query block do not exist: no LSE for them
-      // (their O rows lie outside the tensor map and are not stored)
-      const bool row_exists = !kShortLast || r * kTile + row < p.N;
-      // this warpgroup's columns [w D/2, w D/2 + D/2) of the row go to the
-      // staging buffer: half w for d = 128, units [4w, 4w + 4) of the single
-      // half for d = 64; one thread then stores the tile with TMA, so the
-      // softmax warps issue no global stores of O
-#pragma unroll
-      for (int ch = 0; ch < kOCols / 32; ++ch)
-        tmem_merge_to_stage(tmem + lane_base + col_o(0) + w * kOCols + 32 * ch,
-                            tmem + lane_base + col_o(1) + w * kOCols + 32 * ch, live, f0, f1,
-                            sO + (D == 128 ? w * 16384 : 0), row, D == 128 ? 4 * ch : 4 * w);
       if (ntiles > 0) {
-        // O_0 and O_1 have been read (the loads above completed): the next
-        // item's first products may overwrite them
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar.o_free());
-      }
-      fence_proxy_async_smem();  // the staged rows are read by the TMA engine
-      if (w == 0 && row_exists) {
-        const float m_fin = (m_all == -INFINITY) ? 0.f : m_all;
-        p.lse[it.q_row0 + row] =
-            has ? (m_fin + __log2f(ltot)) * 0.69314718055994531f : -INFINITY;
+        // this item's epilogue runs inside the next item's first step
+        pend = true;
+        pend_m = m;
+        pend_l = l;
+        pend_r = r;
+        pend_bh = bh;
+        pend_jl = J + ntiles - 1;
+      } else {
+        finish(-INFINITY, 0.f, r, bh, 0, 0);  // no key: O = 0, LSE = -inf
       }
       J += ntiles;
-      // every warp has read the exchange buffer before the next item's
-      // epilogue writes it, and has staged its O rows
-      softmax_bar();
-      if (tid == 0) {
-#pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf)
-          tma_store_3d(&mo, sO + hf * 16384, 64 * hf, r * kTile, bh);
-        bulk_commit_group();
-      }
     }
+    if (pend) finish(pend_m, pend_l, pend_r, pend_bh, 1, pend_jl);
     if (tid == 0) bulk_wait_read_all();  // the last O stores, before the CTA exits
   }
 
