@@ -131,14 +131,20 @@ size_t flashmask_workspace_bytes(int B, int H, int Hm, int N, int d, int for_bwd
 fm_status flashmask_workspace_layout(int B, int H, int Hm, int N, int d, int for_bwd,
                                      fm_ws_layout* out);
 
-/* Tile classification pre-pass: reduces the boundary vectors to the per-key-block
- * min/max table, the exact three-way label of every (query block, key block)
- * tile, the compacted non-FULL lists and the descending-work orders, all in the
- * workspace. Reads 16*B*Hm*N bytes. Asynchronous on `stream`. */
+/* Tile classification pre-pass ("FlashMask" abstract: the column-wise
+ * representation lets whole masked blocks be skipped; "FlashMask-3" abstract:
+ * the four boundary vectors): reduces the boundary vectors to the
+ * per-key-block min/max table, the exact three-way label of every (query
+ * block, key block) tile, the compacted non-FULL lists and the
+ * descending-work orders, all in the workspace. Reads 16*B*Hm*N bytes.
+ * Asynchronous on `stream`. */
 fm_status flashmask_classify(const fm_mask* mask, int B, int N, void* ws, size_t ws_bytes,
                              void* stream);
 
-/* Forward: O [B,H,N,d] bf16 and LSE [B,H,N] fp32 from Q, K, V. `scale`
+/* Forward ("FlashMask" abstract: exact attention under the column-wise mask,
+ * masked tiles skipped; "FlashAttention-3" abstract: the block-wise matmuls
+ * overlapped with the softmax): O [B,H,N,d] bf16 and LSE [B,H,N] fp32 from
+ * Q, K, V, as defined at the top of this file. `scale`
  * multiplies Q K^T (pass 1/sqrt(d) for standard attention). If
  * ws_classified == 0 the call runs flashmask_classify first; pass 1 to reuse a
  * classification of the same mask already in `ws`. Asynchronous on `stream`.
@@ -151,8 +157,10 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
                         int H, int N, int d, float scale, void* o, float* lse, void* ws,
                         size_t ws_bytes, int ws_classified, void* stream);
 
-/* Backward: dQ, dK, dV [B,H,N,d] bf16 from Q, K, V, the forward's O and LSE,
- * and the upstream gradient dO. The workspace must be sized with for_bwd != 0.
+/* Backward ("FlashMask" abstract: exact gradients under the same mask, masked
+ * tiles skipped; the FlashAttention README: P recomputed from Q, K and the
+ * saved statistics instead of stored): dQ, dK, dV [B,H,N,d] bf16 from Q, K,
+ * V, the forward's O and LSE, and the upstream gradient dO. The workspace must be sized with for_bwd != 0.
  * ws_classified as in flashmask_fwd. Asynchronous on `stream`. The main
  * kernel gives each (head, key block) one CTA, except that with Tc >= 512 key
  * blocks (the environment variable FM_BWD_SPLIT_MIN_BLOCKS changes 512), among
