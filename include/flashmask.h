@@ -158,9 +158,10 @@ fm_status flashmask_fwd(const void* q, const void* k, const void* v, const fm_ma
                         size_t ws_bytes, int ws_classified, void* stream);
 
 /* Backward ("FlashMask" abstract: exact gradients under the same mask, masked
- * tiles skipped; the FlashAttention README: P recomputed from Q, K and the
- * saved statistics instead of stored): dQ, dK, dV [B,H,N,d] bf16 from Q, K,
- * V, the forward's O and LSE, and the upstream gradient dO. The workspace must be sized with for_bwd != 0.
+ * tiles skipped; the FlashAttention README's memory savings, read here as P
+ * recomputed from Q, K and the saved LSE rather than stored): dQ, dK, dV
+ * [B,H,N,d] bf16 from Q, K, V, the forward's O and LSE, and the upstream
+ * gradient dO. The workspace must be sized with for_bwd != 0.
  * ws_classified as in flashmask_fwd. Asynchronous on `stream`. The main
  * kernel gives each (head, key block) one CTA, except that with Tc >= 512 key
  * blocks (the environment variable FM_BWD_SPLIT_MIN_BLOCKS changes 512), among
