@@ -674,38 +674,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c_row = kFp8 ? p.scale_log2 * p.qscale[static_cast<size_t>(bh) * p.Tr + r]
                                : p.scale_log2;
       float m = -INFINITY, l = 0.f;
-      int next_entry = it.first;  // list entries read one step ahead
+      // The element mask applies on PARTIAL tiles and on every tile of a short
+      // last key block (its keys >= N do not exist and are masked). Lane l
+      // needs the bounds of key columns 64w + l and 64w + 32 + l of a masked
+      // step's block; they are loaded one step ahead (and the list entries
+      // two steps ahead), so that their latency hides behind a step.
+      auto masked_step = [&](int e) {
+        return (e & 3) == FM_TILE_PARTIAL || (kShortLast && (e >> 2) == p.Tc - 1);
+      };
+      auto load_bounds = [&](int e, int (&bd)[8]) {
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int jc = (e >> 2) * kTile + 64 * w + 32 * kk + lane;
+          bd[4 * kk] = bd[4 * kk + 1] = bd[4 * kk + 2] = bd[4 * kk + 3] = 0;
+          if (!kShortLast || jc < p.N) {
+            const size_t col = static_cast<size_t>(bm) * p.N + jc;
+            bd[4 * kk] = p.mask.lts[col];
+            bd[4 * kk + 1] = p.mask.lte[col];
+            bd[4 * kk + 2] = p.mask.uts ? p.mask.uts[col] : 0;
+            bd[4 * kk + 3] = p.mask.ute ? p.mask.ute[col] : 0;
+          }
+        }
+      };
+      int ent_nxt = ntiles > 1 ? it.list[1] : 0;  // the entry of step j + 1
+      int bnd[8] = {0, 0, 0, 0, 0, 0, 0, 0};       // bounds of step j
+      if (ntiles > 0 && masked_step(it.first)) load_bounds(it.first, bnd);
+      int entry_cur = it.first;
       for (int j = 0; j < ntiles; ++j) {
         const int Jj = J + j;
-        const int entry = next_entry;
-        if (j + 1 < ntiles) next_entry = it.list[j + 1];
+        const int entry = entry_cur;
+        int bnd_nxt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (j + 1 < ntiles && masked_step(ent_nxt)) load_bounds(ent_nxt, bnd_nxt);
+        const int ent_nn = j + 2 < ntiles ? it.list[j + 2] : 0;
         const int g = Jj % kSRegions;
         const float c =
             kFp8 ? c_row * p.kscale[static_cast<size_t>(bh) * p.Tc + (entry >> 2)] : c_row;
-        // The element mask applies on PARTIAL tiles and on every tile of a short
-        // last key block (its keys >= N do not exist and are masked).
-        const bool short_keys = kShortLast && (entry >> 2) == p.Tc - 1;
-        const bool partial = (entry & 3) == FM_TILE_PARTIAL || short_keys;
+        const bool partial = masked_step(entry);
         // lane l builds the masked-row bits of key column 64w + 32k + l for this
         // warp's 32 rows; a bit transpose hands each lane its own row's bits
-        // over those 32 columns. The bound loads overlap the wait for S.
+        // over those 32 columns
         uint32_t mbits[2] = {0u, 0u};
         if (partial) {
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
             const int jc = (entry >> 2) * kTile + 64 * w + 32 * kk + lane;
             uint32_t colbits = 0xffffffffu;  // a key >= N masks every row
-            if (!kShortLast || jc < p.N) {
-              const size_t col = static_cast<size_t>(bm) * p.N + jc;
-              const int lts = p.mask.lts[col], lte = p.mask.lte[col];
-              const int uts = p.mask.uts ? p.mask.uts[col] : 0;
-              const int ute = p.mask.ute ? p.mask.ute[col] : 0;
-              colbits = column_mask_bits(jc, lts, lte, uts, ute, p.mask.causal != 0,
+            if (!kShortLast || jc < p.N)
+              colbits = column_mask_bits(jc, bnd[4 * kk], bnd[4 * kk + 1], bnd[4 * kk + 2],
+                                         bnd[4 * kk + 3], p.mask.causal != 0,
                                          r * kTile + 32 * (warp & 3));
-            }
             mbits[kk] = warp_transpose_bits(colbits);
           }
         }
+        entry_cur = ent_nxt;
+        ent_nxt = ent_nn;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) bnd[i] = bnd_nxt[i];
         if (ok) {
           ok = __all_sync(0xffffffffu,
                           mbar_wait(bar.s_full(g), (Jj / kSRegions) & 1, p.status));
