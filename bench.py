@@ -59,7 +59,7 @@ E2E_CHUNK_HEADS = 2
 # so traffic grows in proportion to the heads.
 NCU_TRAFFIC = {
     "bwd_main@cfd872d4df87@document_b1h32n32768d128": 4 * (410.560512e6 + 221.885184e6),
-    "fwd@e40306af048d@document_b1h32n32768d128": 4 * (206.305536e6 + 164.823808e6),
+    "fwd@0d685135e61b@document_b1h32n32768d128": 4 * (202.532352e6 + 163.970560e6),
 }
 
 
